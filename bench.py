@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Benchmark of the low-bit all-reduce hot path on GB300.
+
+One step = a simulated W=8 low-bit all-reduce of a GPT-1.3B-shaped flat
+gradient (8 rank arrays of 1.3e9 bf16 elements, N(0, 1e-3^2), per-rank seeds)
+on one GPU:
+  stage 1  8 encoder launches (4-bit, block 128, round to nearest, error
+           feedback): read g (bf16) + e, write e', codes, fp16 scales;
+  stage 2  8 chunk decoder launches (chunk c = blocks [c*ceil(nb/8), ...)):
+           unpack + dequantise the 8 ranks' codes, rank-ordered fp32 sum,
+           stage-2 error feedback, requantise to 4 bits, repack.
+Metric: GB/s of gradient input processed, counted as fp32 (4 bytes per
+element of the 8 ranks), plus the dominant kernel's fraction of the measured
+HBM copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU (the ranks are independent problems): value = all ranks' elements /
+the slowest rank's time.  --impl reference times the CPU oracle (single
+thread) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantize-pack & unpack-reduce-requant GB/s of fp32 input; % of HBM roofline"
+UNIT = "GB/s"
+WORKLOAD = "allreduce_w8_gpt1p3b"
+W_RANKS = 8
+N_PER_RANK = 1_300_000_000
+BITS, BLOCK = 4, 128
+ENC_BYTES_PER_ELEM = 2 + 4 + 4 + BITS / 8 + 2 / BLOCK           # g bf16, e in, e' out, codes, scales
+DEC_BYTES_PER_ELEM = W_RANKS * (BITS / 8 + 2 / BLOCK) + 4 + 4 + BITS / 8 + 2 / BLOCK  # W inputs, e2 r/w, out
+
+# DRAM traffic per element measured by ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum over the captured launch / its elements), valid only
+# while the kernel sources hash to `src`.  Filled from profiles/.
+NCU_TRAFFIC = {}
+
+
+def kernel_src_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_gradient_communication_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class AllReduceW8:
+    """Device buffers and the launch sequence of one simulated all-reduce."""
+
+    def __init__(self, torch, bc, synth, n, W, device):
+        self.torch, self.bc, self.n, self.W = torch, bc, n, W
+        self.p1 = [bc.QParams(BITS, BLOCK, bc.RTN, seed=1000 + w) for w in range(W)]
+        self.p2 = bc.QParams(BITS, BLOCK, bc.RTN, philox_stream=1)
+        self.x = [synth.gradients("normal", n, 1000 + w, dtype=torch.bfloat16, device=device, sigma=1e-3)
+                  for w in range(W)]
+        self.err = [torch.zeros(n, dtype=torch.float32, device=device) for _ in range(W)]
+        self.codes, self.scales = zip(*[bc.alloc_codes(n, self.p1[0], device) for _ in range(W)])
+        self.err2 = torch.zeros(n, dtype=torch.float32, device=device)
+        self.codes_out, self.scales_out = bc.alloc_codes(n, self.p2, device)
+        nb = bc.num_blocks(n, BLOCK)
+        cb = (nb + W - 1) // W
+        self.chunks = []
+        for c in range(W):
+            b0, b1 = c * cb, min((c + 1) * cb, nb)
+            if b0 >= b1:
+                break
+            lo, hi = b0 * BLOCK, min(b1 * BLOCK, n)
+            self.chunks.append((lo, hi, b0, b1))
+
+    def encode(self, stream=None):
+        for w in range(self.W):
+            self.bc.quantize_pack(self.x[w], self.p1[w], self.err[w], self.codes[w], self.scales[w],
+                                  stream=stream)
+
+    def encode_rank(self, w, stream=None):
+        self.bc.quantize_pack(self.x[w], self.p1[w], self.err[w], self.codes[w], self.scales[w],
+                              stream=stream)
+
+    def decode(self, stream=None):
+        cbytes = BITS // 2 if BITS >= 2 else 1
+        for lo, hi, b0, b1 in self.chunks:
+            cin = [c[lo * BITS // 8: b1 * BLOCK * BITS // 8] for c in self.codes]
+            sin = [s[b0:b1] for s in self.scales]
+            self.bc.unpack_dequant_reduce_requant(
+                cin, sin, hi - lo, self.p1[0], sum_out=None, err2=self.err2[lo:hi],
+                p_out=self.p2.shifted(lo), codes_out=self.codes_out[lo * BITS // 8: b1 * BLOCK * BITS // 8],
+                scales_out=self.scales_out[b0:b1], stream=stream)
+        del cbytes
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import bit_gradient_communication_gb300 as bc
+    from bit_gradient_communication_gb300 import _build, synth
+
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    n, W = args.n, W_RANKS
+
+    # CPU baseline first (the oracle is single threaded, rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(torch, synth, args.cpu_sample)
+
+    ar = AllReduceW8(torch, bc, synth, n, W, dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        ar.encode()
+        ar.decode()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for k in range(K):
+        ev[k][0].record(stream)
+        ar.encode()
+        ev[k][1].record(stream)
+        ar.decode()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    enc_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    step_ms = total_ms / K
+
+    # end to end: pinned host gradients -> device, the step, requantised result -> host
+    e2e = run_e2e(torch, bc, ar, args, dev) if not args.no_e2e else None
+    if world > 1:
+        t = torch.tensor([e2e["step_ms"] if e2e else 0.0], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        if e2e:
+            e2e["step_ms"] = float(t.item())
+
+    if rank != 0:
+        return
+    elems = W * n * world
+    value = elems * 4 / (step_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak_gbs()
+    enc_launch_s = enc_ms / W * 1e-3
+    dec_launch_s = dec_ms / len(ar.chunks) * 1e-3
+    enc_bytes = n * ENC_BYTES_PER_ELEM
+    dec_bytes = (n / len(ar.chunks)) * DEC_BYTES_PER_ELEM
+    enc_gbs = enc_bytes / enc_launch_s / 1e9
+    dec_gbs = dec_bytes / dec_launch_s / 1e9
+    src = kernel_src_hash()
+    tr = NCU_TRAFFIC.get("encode")
+    traffic = tr["bytes_per_elem"] * n if tr and tr["src"] == src else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "ranks_simulated": W, "elements_per_rank": n,
+                   "input_dtype": "bf16", "bits": BITS, "block": BLOCK, "rounding": "rtn",
+                   "error_feedback": "stage1+stage2", "chunks": len(ar.chunks),
+                   "l2": "inputs larger than L2 (%.1f GB of gradients per step)" % (W * n * 2 / 1e9),
+                   "input_gbs_bf16": round(W * n * 2 * world / (step_ms * 1e-3) / 1e9, 2),
+                   "parallelism": "replicas" if world > 1 else "single-gpu"},
+        "roofline": {"bound": "hbm", "kernel": "encode_kernel<bf16,4,ef,rtn>",
+                     "achieved": round(enc_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(enc_gbs / peak, 4), "peak_kind": peak_kind,
+                     "traffic": traffic, "bytes_per_launch": enc_bytes,
+                     "launch_ms": round(enc_launch_s * 1e3, 4)},
+        "kernels": {
+            "encode": {"gbs": round(enc_gbs, 1), "frac": round(enc_gbs / peak, 4),
+                       "launch_ms": round(enc_launch_s * 1e3, 4), "bytes_per_elem": ENC_BYTES_PER_ELEM},
+            "decode_w8": {"gbs": round(dec_gbs, 1), "frac": round(dec_gbs / peak, 4),
+                          "launch_ms": round(dec_launch_s * 1e3, 4), "bytes_per_elem": DEC_BYTES_PER_ELEM},
+        },
+        "gpu_launches": K * (W + len(ar.chunks)),
+        "clocks": clk,
+        "kernel_src": src,
+    }
+    if e2e:
+        line["e2e"] = {"value": round(elems * 4 / (e2e["step_ms"] * 1e-3) / 1e9, 2), "unit": UNIT,
+                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                       "ms_per_step": round(e2e["step_ms"], 3)}
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(torch, bc, ar, args, dev):
+    """Host -> device copies of the 8 ranks' gradients (pinned), the step, and
+    the requantised codes + scales back to the host, all inside the timed
+    region.  Rank w's copy runs on a copy stream and overlaps rank w-1's
+    encoder."""
+    W, n = ar.W, ar.n
+    host_x = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(W)]
+    for w in range(W):
+        host_x[w].copy_(ar.x[w])
+    host_codes = torch.empty(ar.codes_out.numel(), dtype=torch.uint8, pin_memory=True)
+    host_scales = torch.empty(ar.scales_out.numel(), dtype=torch.int16, pin_memory=True)
+    compute = torch.cuda.current_stream()
+    copy = torch.cuda.Stream(device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host_x)
+    d2h = host_codes.numel() + host_scales.numel() * 2
+
+    def step():
+        done = []
+        for w in range(W):
+            copy.wait_stream(compute) if w == 0 else None
+            with torch.cuda.stream(copy):
+                ar.x[w].copy_(host_x[w], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(copy)
+            done.append(e)
+        for w in range(W):
+            compute.wait_event(done[w])
+            ar.encode_rank(w)
+        ar.decode()
+        host_codes.copy_(ar.codes_out, non_blocking=True)
+        host_scales.copy_(ar.scales_out, non_blocking=True)
+
+    steps = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(compute)
+    for _ in range(steps):
+        step()
+    t1.record(compute)
+    torch.cuda.synchronize()
+    return {"step_ms": t0.elapsed_time(t1) / steps, "h2d": h2d, "d2h": d2h}
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_sample_step(O, xs_bits, S):
+    """One sampled step on the host: 8 rank encoders over S elements each,
+    then the W=8 decoder over the same S elements (one chunk)."""
+    import numpy as np
+    p1 = O.params(BITS, BLOCK)
+    enc = []
+    t0 = time.perf_counter()
+    for w in range(W_RANKS):
+        e = np.zeros(S, np.float32)
+        enc.append(O.quantize_pack(xs_bits[w], p1, e))
+    e2 = np.zeros(S, np.float32)
+    O.unpack_dequant_reduce_requant([c for c, _ in enc], [s for _, s in enc], S, p1, False, e2,
+                                    O.params(BITS, BLOCK, philox_stream=1))
+    return time.perf_counter() - t0
+
+
+def _sample_inputs(S):
+    import numpy as np
+
+    from bit_gradient_communication_gb300 import synth
+    xs = []
+    for w in range(W_RANKS):
+        x = synth.np_gradients("normal", S, 1000 + w, sigma=1e-3)
+        # bf16 bits by round-to-nearest-even of the fp32 draw (host-side input recipe)
+        u = x.view(np.uint32).astype(np.uint64)
+        u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+        xs.append(u.astype(np.uint16))
+    return xs
+
+
+def cpu_baseline_sample(torch, synth, S):
+    import oracle as O
+    O.build()
+    xs = _sample_inputs(S)
+    t = _oracle_sample_step(O, xs, S)
+    return {"value": round(W_RANKS * S * 4 / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"8 rank encoders over {S} bf16 elements each + the W=8 decoder over "
+                      f"{S} elements (one chunk), single-threaded C++ oracle, {t:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle as O
+    O.build()
+    S = args.ref_sample
+    xs = _sample_inputs(S)
+    for _ in range(args.warmup):
+        _oracle_sample_step(O, xs, S)
+    ts = [_oracle_sample_step(O, xs, S) for _ in range(args.steps)]
+    t = sum(ts) / len(ts)
+    value = W_RANKS * S * 4 / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "ranks_simulated": W_RANKS, "elements_per_rank": args.n,
+                   "input_dtype": "bf16", "bits": BITS, "block": BLOCK, "rounding": "rtn",
+                   "error_feedback": "stage1+stage2",
+                   "sample_elements_per_rank": S},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"per step: 8 rank encoders over {S} bf16 elements + the W=8 "
+                                   f"decoder over {S} elements, single-threaded C++ oracle"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--n", type=int, default=N_PER_RANK, help="elements per simulated rank")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-sample", type=int, default=1 << 23)
+    ap.add_argument("--ref-sample", type=int, default=1 << 21)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+// api.cpp -- the C ABI entry points of include/bitscom.h: host-side argument
+// checks (nothing is enqueued on a bad argument), then one kernel launch each.
+#include "bitscom.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "launch.h"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+bitscom_status cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return BITSCOM_OK;
+    if (e == cudaErrorNotSupported) return BITSCOM_EUNSUPPORTED;
+    std::strncpy(g_last_cuda_error, cudaGetErrorString(e), sizeof(g_last_cuda_error) - 1);
+    return BITSCOM_ECUDA;
+}
+
+bool valid_bits(int b) { return b == 1 || b == 2 || b == 4 || b == 8 || b == 12 || b == 16; }
+
+int log2_block(int B)
+{
+    if (B < 8 || B > 4096 || (B & (B - 1)) != 0) return -1;
+    int l = 0;
+    while ((1 << l) < B) ++l;
+    return l;
+}
+
+bool valid_params(const bitscom_qparams* p)
+{
+    return p && valid_bits(p->bits) && log2_block(p->block) >= 0 &&
+           (p->rounding == BITSCOM_RTN || p->rounding == BITSCOM_SR);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Width of one thread's code store/load: 8 codes = b bytes.
+uintptr_t code_align(int bits)
+{
+    switch (bits) {
+    case 1: return 1;
+    case 2: return 2;
+    case 4: return 4;
+    case 8: return 8;
+    case 12: return 4;
+    default: return 16;
+    }
+}
+
+}  // namespace
+
+namespace bitscom {
+
+bitscom_status check_encode(const void* x, bitscom_dtype dt, int64_t n, const float* err,
+                            const bitscom_qparams* p, const void* codes, const uint16_t* scales)
+{
+    if (!valid_params(p) || n < 0 || (dt != BITSCOM_F32 && dt != BITSCOM_BF16)) return BITSCOM_EINVAL;
+    if (n == 0) return BITSCOM_OK;
+    if (!x || !codes || !scales) return BITSCOM_EINVAL;
+    if (!aligned(x, dt == BITSCOM_F32 ? 32 : 16) || (err && !aligned(err, 32)) ||
+        !aligned(codes, code_align(p->bits)) || !aligned(scales, 2))
+        return BITSCOM_EALIGN;
+    return BITSCOM_OK;
+}
+
+bitscom_status check_decode(const void* const* codes_in, const uint16_t* const* scales_in, int32_t W,
+                            int64_t n, const bitscom_qparams* p_in, const float* sum_out,
+                            const float* err2, const bitscom_qparams* p_out, const void* codes_out,
+                            const uint16_t* scales_out)
+{
+    if (!valid_params(p_in) || n < 0 || W < 1 || W > kMaxRanks) return BITSCOM_EINVAL;
+    if (p_out && !valid_params(p_out)) return BITSCOM_EINVAL;
+    if (err2 && !p_out) return BITSCOM_EINVAL;
+    if (!sum_out && !p_out) return BITSCOM_EINVAL;
+    if (n == 0) return BITSCOM_OK;
+    if (!codes_in || !scales_in) return BITSCOM_EINVAL;
+    if (p_out && (!codes_out || !scales_out)) return BITSCOM_EINVAL;
+    for (int w = 0; w < W; ++w) {
+        if (!codes_in[w] || !scales_in[w]) return BITSCOM_EINVAL;
+        if (!aligned(codes_in[w], code_align(p_in->bits)) || !aligned(scales_in[w], 2)) return BITSCOM_EALIGN;
+    }
+    if ((sum_out && !aligned(sum_out, 32)) || (err2 && !aligned(err2, 32))) return BITSCOM_EALIGN;
+    if (p_out && (!aligned(codes_out, code_align(p_out->bits)) || !aligned(scales_out, 2))) return BITSCOM_EALIGN;
+    return BITSCOM_OK;
+}
+
+const char* record_cuda_error(cudaError_t e)
+{
+    std::strncpy(g_last_cuda_error, cudaGetErrorString(e), sizeof(g_last_cuda_error) - 1);
+    return g_last_cuda_error;
+}
+
+}  // namespace bitscom
+
+extern "C" {
+
+int64_t bitscom_num_blocks(int64_t n, int32_t block)
+{
+    if (n < 0 || block <= 0) return -1;
+    return (n + block - 1) / block;
+}
+
+int64_t bitscom_packed_bytes(int64_t n, int32_t bits, int32_t block)
+{
+    if (n < 0 || block <= 0 || !valid_bits(bits)) return -1;
+    return (n + block - 1) / block * block * bits / 8;
+}
+
+const char* bitscom_status_string(bitscom_status s)
+{
+    switch (s) {
+    case BITSCOM_OK: return "ok";
+    case BITSCOM_EINVAL: return "invalid argument";
+    case BITSCOM_EALIGN: return "pointer not aligned";
+    case BITSCOM_EUNSUPPORTED: return "unsupported combination";
+    case BITSCOM_ECUDA: return "CUDA error";
+    case BITSCOM_ETIMEOUT: return "timed out";
+    default: return "unknown status";
+    }
+}
+
+const char* bitscom_last_cuda_error(void) { return g_last_cuda_error; }
+
+bitscom_status bitscom_quantize_pack(const void* x, bitscom_dtype dt, int64_t n, float* err,
+                                     const bitscom_qparams* p, void* codes_out,
+                                     uint16_t* scales_out, void* cuda_stream)
+{
+    const bitscom_status chk = bitscom::check_encode(x, dt, n, err, p, codes_out, scales_out);
+    if (chk != BITSCOM_OK || n == 0) return chk;
+    bitscom::EncArgs a;
+    a.x = x;
+    a.err = err;
+    a.n = n;
+    a.log2B = log2_block(p->block);
+    a.nb = (n + p->block - 1) / p->block;
+    a.codes = static_cast<uint8_t*>(codes_out);
+    a.scales = scales_out;
+    a.philox_stream = p->philox_stream;
+    a.seed = p->seed;
+    a.index_offset = p->index_offset;
+    return cuda_status(bitscom::launch_encode(a, dt == BITSCOM_F32 ? 0 : 1, p->bits,
+                                              p->rounding == BITSCOM_SR,
+                                              static_cast<cudaStream_t>(cuda_stream)));
+}
+
+bitscom_status bitscom_unpack_dequant_reduce_requant(
+    const void* const* codes_in, const uint16_t* const* scales_in, int32_t W, int64_t n,
+    const bitscom_qparams* p_in, float* sum_out, float* err2, const bitscom_qparams* p_out,
+    void* codes_out, uint16_t* scales_out, void* cuda_stream)
+{
+    const bitscom_status chk = bitscom::check_decode(codes_in, scales_in, W, n, p_in, sum_out, err2,
+                                                     p_out, codes_out, scales_out);
+    if (chk != BITSCOM_OK || n == 0) return chk;
+    bitscom::DecArgs a;
+    std::memset(&a, 0, sizeof(a));
+    for (int w = 0; w < W; ++w) {
+        a.codes[w] = static_cast<const uint8_t*>(codes_in[w]);
+        a.scales[w] = scales_in[w];
+    }
+    a.W = W;
+    a.n = n;
+    a.log2Bin = log2_block(p_in->block);
+    a.log2Bout = p_out ? log2_block(p_out->block) : a.log2Bin;
+    a.nb_out = p_out ? (n + p_out->block - 1) / p_out->block : 0;
+    a.sum_out = sum_out;
+    a.err2 = err2;
+    a.codes_out = static_cast<uint8_t*>(codes_out);
+    a.scales_out = scales_out;
+    if (p_out) {
+        a.philox_stream = p_out->philox_stream;
+        a.seed = p_out->seed;
+        a.index_offset = p_out->index_offset;
+    }
+    return cuda_status(bitscom::launch_decode(a, p_in->bits, p_out ? p_out->bits : 0,
+                                              p_out && p_out->rounding == BITSCOM_SR,
+                                              static_cast<cudaStream_t>(cuda_stream)));
+}
+
+bitscom_status bitscom_roundtrip(const void* x, bitscom_dtype dt, int64_t n, float* err,
+                                 const bitscom_qparams* p, void* codes_tmp,
+                                 uint16_t* scales_tmp, float* deq_out, void* cuda_stream)
+{
+    if (n > 0 && !deq_out) return BITSCOM_EINVAL;
+    if (deq_out && !aligned(deq_out, 32)) return BITSCOM_EALIGN;
+    bitscom_status s = bitscom_quantize_pack(x, dt, n, err, p, codes_tmp, scales_tmp, cuda_stream);
+    if (s != BITSCOM_OK || n == 0) return s;
+    const void* c[1] = {codes_tmp};
+    const uint16_t* sc[1] = {scales_tmp};
+    return bitscom_unpack_dequant_reduce_requant(c, sc, 1, n, p, deq_out, nullptr, nullptr, nullptr,
+                                                 nullptr, cuda_stream);
+}
+
+}  // extern "C"

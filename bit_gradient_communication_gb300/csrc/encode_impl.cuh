@@ -1,0 +1,147 @@
+// encode_impl.cuh -- fused encoder kernel: load g (+ e) -> block statistic ->
+// fp16 scale -> quantise -> pack -> store codes, scales and e'.
+// One pass over the input: every input byte is read once and every output
+// byte written once (bitscom README, "Implemented Features": blockwise
+// quantization with per-block FP16 scales; error-feedback in first-stage
+// quantization).
+#pragma once
+
+#include "codec.cuh"
+#include "launch.h"
+
+namespace bitscom {
+
+// IN: 0 = fp32, 1 = bf16.
+template <int IN, int BITS, bool EF, bool SR>
+__global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
+{
+    __shared__ float red[2][kWarps];
+    const Team team = make_team(a.log2B);
+    const int64_t n = a.n;
+    const int64_t rows = (n + kRow - 1) / kRow;
+    const int64_t padded = a.nb << a.log2B;
+    const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
+    const uint32_t shift = (uint32_t)(a.index_offset & 3u);
+    int parity = 0;
+
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
+        const int64_t e0 = row * kRow + (int64_t)threadIdx.x * kPiece;
+        const int64_t piece = e0 >> 3;
+        const bool full_row = (row + 1) * kRow <= n;
+        int valid = 8;
+        float v[8];
+        if (full_row) {
+            if constexpr (IN == 0) {
+                ld8_f32_stream(static_cast<const float*>(a.x) + e0, v);
+            } else {
+                bf16x8_to_f32(ld16_stream(static_cast<const uint16_t*>(a.x) + e0), v);
+            }
+            if constexpr (EF) {
+                float e[8];
+                ld8_f32(a.err + e0, e);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = __fadd_rn(v[j], e[j]);
+            }
+        } else {
+            const int64_t rem = n - e0;
+            valid = rem <= 0 ? 0 : (rem >= 8 ? 8 : (int)rem);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float g = 0.0f;
+                if (j < valid) {
+                    if constexpr (IN == 0) {
+                        g = static_cast<const float*>(a.x)[e0 + j];
+                    } else {
+                        g = __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[e0 + j] << 16);
+                    }
+                    if constexpr (EF) g = __fadd_rn(g, a.err[e0 + j]);
+                }
+                v[j] = g;
+            }
+        }
+
+        // block statistic: absmax (b >= 2) or tree sum of |v| (b = 1)
+        float stat;
+        if constexpr (BITS == 1) {
+            stat = __fadd_rn(__fadd_rn(__fadd_rn(fabsf(v[0]), fabsf(v[1])), __fadd_rn(fabsf(v[2]), fabsf(v[3]))),
+                             __fadd_rn(__fadd_rn(fabsf(v[4]), fabsf(v[5])), __fadd_rn(fabsf(v[6]), fabsf(v[7]))));
+        } else {
+            stat = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                         fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+        }
+        stat = team_reduce<BITS == 1>(stat, team, red[parity]);
+
+        const int64_t blk = e0 >> a.log2B;
+        int n_valid = 1 << a.log2B;
+        if constexpr (BITS == 1) {
+            const int64_t left = n - (blk << a.log2B);
+            if (left < n_valid) n_valid = left > 0 ? (int)left : 1;
+        }
+        const __half sh = block_scale<BITS>(stat, n_valid);
+        const float s = __half2float(sh);
+
+        uint32_t rw[8];
+        if constexpr (SR && BITS > 1) {
+            random_words8(a.index_offset + (uint64_t)e0, a.philox_stream, k0, k1, shift, rw);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) rw[j] = 0u;
+        }
+        Packed<BITS> c;
+        float q[8];
+        quantize8<BITS, (SR && BITS > 1)>(v, s, rw, c, q);
+
+        if (e0 < padded) store_codes<BITS>(a.codes, piece, c);
+        if (team.lane == 0 && blk < a.nb) a.scales[blk] = __half_as_ushort(sh);
+
+        if constexpr (EF) {
+            float e[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) e[j] = __fsub_rn(v[j], __fmul_rn(s, q[j]));
+            if (valid == 8) {
+                st8_f32(a.err + e0, e);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) if (j < valid) a.err[e0 + j] = e[j];
+            }
+        }
+    }
+}
+
+template <int IN, int BITS, bool EF, bool SR>
+static cudaError_t run_encode(const EncArgs& a, cudaStream_t st)
+{
+    static std::atomic<int> cap{0};   // SMs x resident CTAs of this instantiation
+    const int64_t rows = (a.n + kRow - 1) / kRow;
+    const int grid = grid_size(encode_kernel<IN, BITS, EF, SR>, cap, rows);
+    encode_kernel<IN, BITS, EF, SR><<<grid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int IN, int BITS>
+static cudaError_t encode_bits(const EncArgs& a, bool sr, cudaStream_t st)
+{
+    const bool ef = a.err != nullptr;
+    if constexpr (BITS == 1) {
+        return ef ? run_encode<IN, 1, true, false>(a, st) : run_encode<IN, 1, false, false>(a, st);
+    } else {
+        if (ef) return sr ? run_encode<IN, BITS, true, true>(a, st) : run_encode<IN, BITS, true, false>(a, st);
+        return sr ? run_encode<IN, BITS, false, true>(a, st) : run_encode<IN, BITS, false, false>(a, st);
+    }
+}
+
+template <int IN>
+static cudaError_t encode_dispatch(const EncArgs& a, int bits, bool sr, cudaStream_t st)
+{
+    switch (bits) {
+    case 1: return encode_bits<IN, 1>(a, sr, st);
+    case 2: return encode_bits<IN, 2>(a, sr, st);
+    case 4: return encode_bits<IN, 4>(a, sr, st);
+    case 8: return encode_bits<IN, 8>(a, sr, st);
+    case 12: return encode_bits<IN, 12>(a, sr, st);
+    case 16: return encode_bits<IN, 16>(a, sr, st);
+    default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace bitscom

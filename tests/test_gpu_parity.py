@@ -1,0 +1,214 @@
+"""CUDA path vs the CPU oracle, bit for bit, through the C ABI.
+
+Codes, packed bytes, fp16 scales, error-feedback buffers, rank sums and
+dequantised values must be identical (0 ulp): every fp32 step of the method
+is a fixed sequence of correctly rounded operations.  Sizes span several
+4096-element rows with ragged tails; every output buffer sits between
+sentinel bands that must survive the call.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+from gpu_util import Guarded, bf16_bits_of, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+BITS = [1, 2, 4, 8, 12, 16]
+SIZES = [1, 13, 4096, 3 * 4096 + 40, 5 * 4096 + 1]
+
+
+def _inputs(n, dtype, seed):
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-4, 1)).astype(np.float32)
+    # a few exact zeros, negative zeros and outliers
+    if n > 16:
+        x[rng.integers(0, n, 3)] = 0.0
+        x[rng.integers(0, n, 2)] = -0.0
+        x[rng.integers(0, n, 2)] *= 1000.0
+    e = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    return x, e
+
+
+def _run_encode(torch, bc, x_host, dt, n, p, err_host):
+    """GPU encoder on guarded buffers; returns codes, scales, err (host)."""
+    if dt == "f32":
+        xg = torch.from_numpy(x_host).cuda()
+    else:
+        xg = torch.from_numpy(x_host.view(np.int16)).cuda().view(torch.bfloat16)
+    codes = Guarded(torch, bc.packed_bytes(n, p.bits, p.block))
+    scales = Guarded(torch, 2 * bc.num_blocks(n, p.block))
+    err = Guarded(torch, 4 * n, fill=err_host) if err_host is not None else None
+    bc.quantize_pack(xg, p, err.view(torch.float32) if err else None,
+                     codes.view(torch.uint8), scales.view(torch.int16))
+    torch.cuda.synchronize()
+    assert codes.guards_intact() and scales.guards_intact() and (err is None or err.guards_intact())
+    return codes.host(np.uint8), scales.host(np.uint16), (err.host(np.float32) if err else None)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("bits", BITS)
+@pytest.mark.parametrize("block", [8, 32, 128, 512, 4096])
+@pytest.mark.parametrize("mode", ["rtn", "rtn_ef", "sr", "sr_ef"])
+def test_encoder_matches_oracle(dt, bits, block, mode):
+    torch, bc = need_gpu()
+    sr = mode.startswith("sr")
+    ef = mode.endswith("ef")
+    for k, n in enumerate(SIZES):
+        x, e = _inputs(n, dt, seed=bits * 1000 + block + k)
+        xh = x if dt == "f32" else bf16_bits_of(torch, x)
+        offset = [0, 3, 2 ** 33 + 5, 6, 1][k]
+        p = bc.QParams(bits, block, bc.SR if sr else bc.RTN, seed=0x1234_5678_9ABC + k,
+                       index_offset=offset, philox_stream=k & 1)
+        po = O.params(bits, block, O.SR if sr else O.RTN, seed=p.seed, index_offset=offset,
+                      philox_stream=p.philox_stream)
+        codes, scales, err = _run_encode(torch, bc, xh, dt, n, p, e.copy() if ef else None)
+        e_ref = e.copy() if ef else None
+        c_ref, s_ref = O.quantize_pack(xh, po, e_ref)
+        assert codes.tobytes() == c_ref.tobytes(), f"codes differ at n={n}"
+        assert np.array_equal(scales, s_ref), f"scales differ at n={n}"
+        if ef:
+            assert np.array_equal(err.view(np.uint32), e_ref.view(np.uint32)), f"e' differs at n={n}"
+
+
+def test_encoder_is_deterministic():
+    torch, bc = need_gpu()
+    n = 7 * 4096 + 3
+    x, e = _inputs(n, "f32", 5)
+    p = bc.QParams(4, 128, bc.SR, seed=7)
+    a = _run_encode(torch, bc, x, "f32", n, p, e.copy())
+    b = _run_encode(torch, bc, x, "f32", n, p, e.copy())
+    assert a[0].tobytes() == b[0].tobytes() and np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+
+
+def test_encoder_special_blocks():
+    # zero blocks, underflowing and subnormal scales, saturation, negative zero
+    torch, bc = need_gpu()
+    n = 4096
+    x = np.zeros(n, np.float32)
+    x[128:256] = 2.0 ** -26          # absmax/7 underflows fp16 -> s = 0
+    x[256:384] = 3 * 2.0 ** -24 * 7  # subnormal scale
+    x[384:512] = 1e6                 # saturated scale
+    x[512] = -0.0
+    x[640:768] = np.linspace(-3, 3, 128)
+    for bits in BITS:
+        for ef in (False, True):
+            e = np.zeros(n, np.float32)
+            p = bc.QParams(bits, 128)
+            codes, scales, err = _run_encode(torch, bc, x, "f32", n, p, e.copy() if ef else None)
+            e_ref = e.copy() if ef else None
+            c_ref, s_ref = O.quantize_pack(x, O.params(bits, 128), e_ref)
+            assert codes.tobytes() == c_ref.tobytes() and np.array_equal(scales, s_ref)
+            if ef:
+                assert np.array_equal(err.view(np.uint32), e_ref.view(np.uint32))
+
+
+def _random_codes(rng, n, bits, block, scale_sigma=1e-3):
+    nbytes = O.packed_bytes(n, bits, block)
+    codes = rng.integers(0, 256, nbytes, dtype=np.uint8)
+    s = np.abs(rng.standard_normal(O.num_blocks(n, block)) * scale_sigma).astype(np.float16)
+    s[rng.integers(0, s.size, max(1, s.size // 50))] = 0.0
+    return codes, s.view(np.uint16)
+
+
+DEC_CASES = [(b, 0, 128, 128) for b in BITS] + [(b, b, 128, 128) for b in BITS] + \
+            [(b, b, B, B) for b in (1, 4, 16) for B in (8, 32, 512, 4096)] + \
+            [(8, 4, 512, 128), (8, 4, 128, 512), (8, 4, 32, 4096)]
+
+
+@pytest.mark.parametrize("bin_,bout,Bin,Bout", DEC_CASES)
+@pytest.mark.parametrize("W", [1, 3, 8, 9])
+@pytest.mark.parametrize("mode", ["plain", "ef2", "sr_ef2"])
+def test_decoder_matches_oracle(bin_, bout, Bin, Bout, W, mode):
+    torch, bc = need_gpu()
+    if bout == 0 and mode != "plain":
+        pytest.skip("stage-2 options need requantisation")
+    rng = np.random.default_rng(bin_ * 7919 + bout * 31 + W + Bin + Bout)
+    for n in (5, 4096 + 8, 3 * 4096 + 77):
+        ins = [_random_codes(rng, n, bin_, Bin) for _ in range(W)]
+        pin = bc.QParams(bin_, Bin)
+        sr = mode == "sr_ef2"
+        pout = bc.QParams(bout, Bout, bc.SR if sr else bc.RTN, seed=99, index_offset=2 ** 32 + 1,
+                          philox_stream=1) if bout else None
+        e2 = (rng.standard_normal(n) * 1e-3).astype(np.float32) if mode != "plain" else None
+
+        cin = [Guarded(torch, c.size, fill=c) for c, _ in ins]
+        sin = [Guarded(torch, 2 * s.size, fill=s) for _, s in ins]
+        sum_g = Guarded(torch, 4 * n)
+        e2_g = Guarded(torch, 4 * n, fill=e2) if e2 is not None else None
+        co = Guarded(torch, bc.packed_bytes(n, bout, Bout)) if bout else None
+        so = Guarded(torch, 2 * bc.num_blocks(n, Bout)) if bout else None
+        bc.unpack_dequant_reduce_requant(
+            [c.view(torch.uint8) for c in cin], [s.view(torch.int16) for s in sin], n, pin,
+            sum_out=sum_g.view(torch.float32), err2=e2_g.view(torch.float32) if e2_g else None,
+            p_out=pout, codes_out=co.view(torch.uint8) if co else None,
+            scales_out=so.view(torch.int16) if so else None)
+        torch.cuda.synchronize()
+        for g in [sum_g, e2_g, co, so] + cin + sin:
+            assert g is None or g.guards_intact()
+
+        po = O.params(bout, Bout, O.SR if sr else O.RTN, seed=99, index_offset=2 ** 32 + 1,
+                      philox_stream=1) if bout else None
+        e2_ref = e2.copy() if e2 is not None else None
+        s_ref, c_ref, sc_ref = O.unpack_dequant_reduce_requant(
+            [c for c, _ in ins], [s for _, s in ins], n, O.params(bin_, Bin), True, e2_ref, po)
+        assert np.array_equal(sum_g.host(np.uint32), s_ref.view(np.uint32)), f"sum differs n={n}"
+        if bout:
+            assert co.host(np.uint8).tobytes() == c_ref.tobytes(), f"codes differ n={n}"
+            assert np.array_equal(so.host(np.uint16), sc_ref), f"scales differ n={n}"
+        if e2 is not None:
+            assert np.array_equal(e2_g.host(np.uint32), e2_ref.view(np.uint32)), f"e2' differs n={n}"
+
+
+def test_decoder_requant_without_sum_output():
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(11)
+    n, W = 2 * 4096 + 9, 4
+    ins = [_random_codes(rng, n, 4, 128) for _ in range(W)]
+    cin = [torch.from_numpy(c).cuda() for c, _ in ins]
+    sin = [torch.from_numpy(s.view(np.int16)).cuda() for _, s in ins]
+    p = bc.QParams(4, 128)
+    _, co, so = bc.unpack_dequant_reduce_requant(cin, sin, n, p, sum_out=None, p_out=p)
+    _, c_ref, s_ref = O.unpack_dequant_reduce_requant([c for c, _ in ins], [s for _, s in ins], n,
+                                                      O.params(4, 128), False, None, O.params(4, 128))
+    assert co.cpu().numpy().tobytes() == c_ref.tobytes()
+    assert np.array_equal(so.cpu().numpy().view(np.uint16), s_ref)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("bits", BITS)
+def test_roundtrip_matches_oracle(dt, bits):
+    torch, bc = need_gpu()
+    n = 3 * 4096 + 5
+    x, e = _inputs(n, dt, bits)
+    xh = x if dt == "f32" else bf16_bits_of(torch, x)
+    xg = torch.from_numpy(xh if dt == "f32" else xh.view(np.int16)).cuda()
+    if dt == "bf16":
+        xg = xg.view(torch.bfloat16)
+    eg = torch.from_numpy(e.copy()).cuda()
+    p = bc.QParams(bits, 128)
+    deq = bc.roundtrip(xg, p, err=eg)
+    e_ref = e.copy()
+    _, _, d_ref = O.roundtrip(xh, O.params(bits, 128), e_ref)
+    torch.cuda.synchronize()
+    assert np.array_equal(deq.cpu().numpy().view(np.uint32), d_ref.view(np.uint32))
+    assert np.array_equal(eg.cpu().numpy().view(np.uint32), e_ref.view(np.uint32))
+
+
+def test_roundtrip_in_place():
+    # deq_out may alias x for fp32 (the simulate-quantization mode)
+    torch, bc = need_gpu()
+    n = 4096 * 2 + 3
+    x, _ = _inputs(n, "f32", 77)
+    xg = torch.from_numpy(x.copy()).cuda()
+    p = bc.QParams(4, 128)
+    bc.roundtrip(xg, p, deq_out=xg)
+    _, _, d_ref = O.roundtrip(x, O.params(4, 128))
+    assert np.array_equal(xg.cpu().numpy().view(np.uint32), d_ref.view(np.uint32))
+
+
+def test_empty_input_is_a_no_op():
+    torch, bc = need_gpu()
+    x = torch.empty(0, device="cuda")
+    codes, scales = bc.quantize_pack(x, bc.QParams(4, 128))
+    assert codes.numel() == 0 and scales.numel() == 0
