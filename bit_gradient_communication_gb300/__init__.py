@@ -97,6 +97,10 @@ def lib():
             L.bitscom_unpack_dequant_reduce_requant.argtypes = [vp, vp, i32, i64, P, vp, vp, P, vp, vp, vp]
             L.bitscom_roundtrip.restype = st
             L.bitscom_roundtrip.argtypes = [vp, st, i64, vp, P, vp, vp, vp, vp]
+            L.bitscom_roundtrip_noalloc.restype = st
+            L.bitscom_roundtrip_noalloc.argtypes = [vp, st, i64, vp, P, vp, vp]
+            L.bitscom_roundtrip_noalloc_max_elements.restype = i64
+            L.bitscom_roundtrip_noalloc_max_elements.argtypes = [i32, i32]
             L.bitscom_sched_create.restype = st
             L.bitscom_sched_create.argtypes = [i32, i64, ctypes.POINTER(vp)]
             L.bitscom_sched_destroy.restype = st
@@ -233,6 +237,29 @@ def roundtrip(x, p: QParams, err=None, codes_tmp=None, scales_tmp=None, deq_out=
                                    ctypes.byref(p.c()), _dev_ptr(codes_tmp, "codes_tmp"),
                                    _dev_ptr(scales_tmp, "scales_tmp"), _dev_ptr(deq_out, "deq_out"),
                                    _stream(stream)), "bitscom_roundtrip")
+    return deq_out
+
+
+def roundtrip_noalloc_max_elements(bits: int, block: int) -> int:
+    return lib().bitscom_roundtrip_noalloc_max_elements(bits, block)
+
+
+def roundtrip_noalloc(x, p: QParams, err=None, deq_out=None, stream=None):
+    """roundtrip() for callers that cannot allocate device memory: the codes and
+    scales go to the library's fixed device scratch (see include/bitscom.h for
+    its capacity and sharing rules).  deq_out must be given by such callers;
+    when it is None this wrapper allocates it for convenience."""
+    torch = _torch()
+    n = x.numel()
+    cap = roundtrip_noalloc_max_elements(p.bits, p.block)
+    if n > cap:
+        raise ValueError(f"n = {n} exceeds the static scratch capacity ({cap} elements for "
+                         f"{p.bits}-bit, block {p.block})")
+    if deq_out is None:
+        deq_out = torch.empty(n, dtype=torch.float32, device=x.device)
+    _check(lib().bitscom_roundtrip_noalloc(_dev_ptr(x, "x"), _dtype_code(x), n, _dev_ptr(err, "err"),
+                                           ctypes.byref(p.c()), _dev_ptr(deq_out, "deq_out"),
+                                           _stream(stream)), "bitscom_roundtrip_noalloc")
     return deq_out
 
 

@@ -38,8 +38,9 @@
  * Memory: the caller allocates and owns every buffer (device memory unless
  * stated) and the CUDA stream.  Calls are asynchronous on the given stream
  * (NULL = legacy default stream); a call enqueues kernels and returns.  The
- * entry points above the scheduler section allocate nothing and keep no
- * state between calls; they may be called from several host threads.
+ * entry points above the scheduler section allocate nothing; except for
+ * bitscom_roundtrip_noalloc (its own rules below) they keep no state between
+ * calls and may be called from several host threads.
  *
  * Errors: arguments are checked on the host before anything is enqueued:
  *   BITSCOM_EINVAL       bits not in {1,2,4,8,12,16}, block not a power of two
@@ -146,6 +147,34 @@ bitscom_status bitscom_unpack_dequant_reduce_requant(
 bitscom_status bitscom_roundtrip(const void* x, bitscom_dtype dt, int64_t n, float* err,
                                  const bitscom_qparams* p, void* codes_tmp,
                                  uint16_t* scales_tmp, float* deq_out, void* cuda_stream);
+
+/*
+ * Allocation-free variant of bitscom_roundtrip (the pages have no counterpart;
+ * this is a library convenience).  For callers that cannot allocate device
+ * memory where they quantise -- e.g. a gradient hook that only holds the
+ * gradient buffer and must not call the CUDA allocator, which can synchronise
+ * the device and compete with a framework's caching allocator.  The codes and
+ * scales live in a fixed device array of this library (8 MiB of codes + 1 MiB
+ * of scales, held on every GPU that loads the library until exit); the caller
+ * still passes x, err and deq_out as in bitscom_roundtrip, and the results are
+ * identical to it.
+ *   - n must not exceed bitscom_roundtrip_noalloc_max_elements(bits, block)
+ *     (at least 4,194,304 for every bits/block; 16,777,216 for 4-bit, block
+ *     128); larger n returns BITSCOM_EINVAL and enqueues nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on the device.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents (nothing in it needs clearing: every code and scale is written
+ *     before it is read).  Calls whose kernels overlap on the GPU race on it.
+ *   - Allocates nothing: no cudaMalloc / cudaFree or allocating library call.
+ */
+bitscom_status bitscom_roundtrip_noalloc(const void* x, bitscom_dtype dt, int64_t n, float* err,
+                                         const bitscom_qparams* p, float* deq_out,
+                                         void* cuda_stream);
+/* Largest n bitscom_roundtrip_noalloc accepts for these parameters (-1 if the
+ * parameters are invalid). */
+int64_t bitscom_roundtrip_noalloc_max_elements(int32_t bits, int32_t block);
 
 /* ------------------------------------------------------------------------
  * Bucket scheduler: splits a flat gradient into fusion buckets (25 MB by
