@@ -154,7 +154,6 @@ class AllReduceW8:
                               stream=stream)
 
     def decode(self, stream=None):
-        cbytes = BITS // 2 if BITS >= 2 else 1
         for lo, hi, b0, b1 in self.chunks:
             cin = [c[lo * BITS // 8: b1 * BLOCK * BITS // 8] for c in self.codes]
             sin = [s[b0:b1] for s in self.scales]
@@ -162,7 +161,6 @@ class AllReduceW8:
                 cin, sin, hi - lo, self.p1[0], sum_out=None, err2=self.err2[lo:hi],
                 p_out=self.p2.shifted(lo), codes_out=self.codes_out[lo * BITS // 8: b1 * BLOCK * BITS // 8],
                 scales_out=self.scales_out[b0:b1], stream=stream)
-        del cbytes
 
 
 def run_ours(args, rank, world, local_rank):
@@ -393,6 +391,138 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# other workloads (python bench.py --workload NAME): one JSON line each
+# ---------------------------------------------------------------------------
+
+def _timed(torch, fn, K, flush=None):
+    """Average device time of fn() over K calls (events on the current stream);
+    flush() runs between calls, outside the timed intervals."""
+    st = torch.cuda.current_stream()
+    total = 0.0
+    for _ in range(K):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        b.record(st)
+        b.synchronize()
+        total += a.elapsed_time(b)
+    return total / K
+
+
+def run_workload(args):
+    import torch
+
+    import bit_gradient_communication_gb300 as bc
+    from bit_gradient_communication_gb300 import _build, synth
+    _build.build()
+    torch.cuda.set_device(0)
+    wl = synth.WORKLOADS[args.workload]
+    peak, peak_kind = measured_peak_gbs()
+    l2_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")   # > 129 MB L2
+
+    def flush():
+        l2_buf.fill_(1)
+
+    K, warm = args.steps, args.warmup
+    lines = []
+    dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+    if args.workload == "sweep_laplace_256m":
+        x = synth.gradients(wl.kind, wl.n, wl.seed, **wl.params)
+        deq = torch.empty(wl.n, device="cuda")
+        for bits in (1, 2, 4, 8, 12, 16):
+            for block in (32, 64, 128, 256, 1024, 4096):
+                for rounding in (bc.RTN, bc.SR):
+                    p = bc.QParams(bits, block, rounding, seed=wl.sr_seed)
+                    codes, scales = bc.alloc_codes(wl.n, p)
+                    enc = lambda: bc.quantize_pack(x, p, None, codes, scales)
+                    dec = lambda: bc.unpack_dequant_reduce_requant([codes], [scales], wl.n, p, sum_out=deq)
+                    for _ in range(warm):
+                        enc()
+                        dec()
+                    te = _timed(torch, enc, K)
+                    td = _timed(torch, dec, K)
+                    cb = bits / 8 + 2 / block
+                    eb, db = wl.n * (4 + cb), wl.n * (cb + 4)
+                    lines.append({"bits": bits, "block": block, "rounding": "sr" if rounding else "rtn",
+                                  "encode_gbs": round(eb / te / 1e6, 1), "encode_frac": round(eb / te / 1e6 / peak, 4),
+                                  "decode_gbs": round(db / td / 1e6, 1), "decode_frac": round(db / td / 1e6 / peak, 4),
+                                  "encode_input_gbs": round(wl.n * 4 / te / 1e6, 1)})
+                    del codes, scales
+        best = max(lines, key=lambda r: r["encode_input_gbs"])
+        head = next(r for r in lines if r["bits"] == 4 and r["block"] == 128 and r["rounding"] == "rtn")
+        out = {"metric": METRIC, "value": head["encode_input_gbs"], "unit": UNIT, "n_gpus": 1, "steps": K,
+               "warmup": warm, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+               "config": {"workload": wl.name, "n": wl.n, "input_dtype": "f32",
+                          "l2": "inputs larger than L2 (1.07 GB)", "value_is": "encoder, 4-bit, block 128, RTN"},
+               "roofline": {"bound": "hbm", "kernel": "encode_kernel<f32,4,noef,rtn>",
+                            "achieved": head["encode_gbs"], "peak": peak, "unit": "GB/s",
+                            "frac": head["encode_frac"], "peak_kind": peak_kind},
+               "best_encode_input_gbs": best["encode_input_gbs"], "sweep": lines}
+        print(json.dumps(out), flush=True)
+        return
+    if args.workload == "roundtrip_1m":
+        x = synth.gradients(wl.kind, wl.n, wl.seed, **wl.params)
+        p = bc.QParams(wl.bits, wl.block)
+        codes, scales = bc.alloc_codes(wl.n, p)
+        deq = torch.empty(wl.n, device="cuda")
+        step = lambda: bc.roundtrip(x, p, None, codes, scales, deq)
+        for _ in range(warm):
+            step()
+        t = _timed(torch, step, K, flush)
+        algo = wl.n * 2 * (4 + wl.bits / 8 + 2 / wl.block)
+        extra = {"l2": "flushed between timed iterations (256 MB write)"}
+    elif args.workload == "bucket25mb_f32":
+        sched = bc.Scheduler(2, wl.bucket_bytes)
+        xs = [synth.gradients(wl.kind, wl.n, t, **wl.params) for t in range(10)]
+        per_bits = {}
+        for bits in (1, 2, 4, 8):
+            err = torch.zeros(wl.n, device="cuda")
+            codes, scales = bc.alloc_codes(wl.n, bc.QParams(bits, wl.block))
+            it = [0]
+
+            def step():
+                t = it[0] % 10
+                sched.quantize_pack(xs[t], bc.QParams(bits, wl.block, wl.rounding, seed=wl.sr_seed,
+                                                      index_offset=t * wl.n), err, codes, scales)
+                it[0] += 1
+            for _ in range(warm):
+                step()
+            tb = _timed(torch, step, K, flush)
+            algo_b = wl.n * (4 + 4 + 4 + bits / 8 + 2 / wl.block)
+            per_bits[bits] = {"ms": round(tb, 4), "input_gbs": round(wl.n * 4 / tb / 1e6, 1),
+                              "gbs": round(algo_b / tb / 1e6, 1), "frac": round(algo_b / tb / 1e6 / peak, 4)}
+        t = per_bits[4]["ms"]
+        algo = wl.n * (12 + 0.5 + 2 / wl.block)
+        extra = {"l2": "flushed between timed iterations (256 MB write)", "per_bits": per_bits,
+                 "value_is": "4-bit"}
+    elif args.workload == "gpt6p7b_2bit_buckets":
+        sched = bc.Scheduler(2, wl.bucket_bytes)
+        x = synth.gradients(wl.kind, wl.n, wl.seed, dtype=dt, **wl.params)
+        err = torch.zeros(wl.n, device="cuda")
+        p = bc.QParams(wl.bits, wl.block, wl.rounding, seed=wl.sr_seed)
+        codes, scales = bc.alloc_codes(wl.n, p)
+        step = lambda: sched.quantize_pack(x, p, err, codes, scales)
+        for _ in range(warm):
+            step()
+        t = _timed(torch, step, K)
+        algo = wl.n * (2 + 8 + wl.bits / 8 + 2 / wl.block)
+        extra = {"l2": "inputs larger than L2 (67 GB per step)", "buckets": 512, "streams": 2}
+    else:
+        raise SystemExit(f"workload {args.workload}: use the default run")
+    gbs = algo / t / 1e6
+    out = {"metric": METRIC, "value": round(wl.n * 4 / t / 1e6, 2), "unit": UNIT, "n_gpus": 1, "steps": K,
+           "warmup": warm, "ms_per_step": round(t, 4), "higher_is_better": True, "dtype": "f32",
+           "data": "synthetic", "config": {"workload": wl.name, "n": wl.n, "input_dtype": wl.dtype,
+                                           "bits": wl.bits, "block": wl.block, **extra},
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind}}
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -405,6 +535,8 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=1 << 21)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="another workload recipe from synth.WORKLOADS (one JSON line of its own)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -414,6 +546,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.workload != WORKLOAD:
+        run_workload(args)
         return
     if world > 1:
         import torch

@@ -1,18 +1,57 @@
-// decode.cu -- fused decoder kernel for one chunk between the all-to-all and
+// decode_impl.cuh -- fused decoder kernel for one chunk between the all-to-all and
 // the all-gather of a low-bit all-reduce: unpack + dequantise the W ranks'
 // codes, sum them in rank order in fp32, optionally add the stage-2 error,
 // requantise + repack (bitscom README, "Implemented Features": all-to-all ->
 // local reduce -> all-gather; "Backend Registration Options":
 // stage2_error_feedback).  Every byte of the W inputs is read once and every
 // output byte written once; the rank sum never leaves registers.
+#pragma once
+
 #include "codec.cuh"
 #include "launch.h"
 
 namespace bitscom {
 
-// BOUT == 0: no requantisation (sum only).
-template <int BIN, int BOUT, bool SR>
-__global__ void __launch_bounds__(kThreads, (BIN >= 12 || BOUT >= 12) ? 1 : 2) decode_kernel(const DecArgs a)
+// One rank's contribution to the 8 running sums: acc = fl(acc + fl(s*q)), or
+// acc = fl(s*q) for the first rank.  For b in {2, 4, 8} the fp16 scale and
+// fp16 levels feed a mixed-precision fma (s*q exact, one rounding); for b = 1
+// and 12 the fp32 fma is exact for the same reason; at b = 16 s*q may need 27
+// bits, so the multiply and the add round separately.
+template <int BITS>
+__device__ __forceinline__ void accumulate_rank(const Packed<BITS>& c, unsigned short sbits, bool first,
+                                                float (&acc)[8])
+{
+    if constexpr (BITS == 2 || BITS == 4 || BITS == 8) {
+        uint32_t h[4];
+        level_pairs<BITS>(c, h);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int jl = pair_lo<BITS>(i), jh = pair_hi<BITS>(i);
+            const unsigned short ql = (unsigned short)(h[i] & 0xFFFFu), qh = (unsigned short)(h[i] >> 16);
+            acc[jl] = fma_f16(sbits, ql, first ? -0.0f : acc[jl]);
+            acc[jh] = fma_f16(sbits, qh, first ? -0.0f : acc[jh]);
+        }
+    } else {
+        const float s = __half2float(__ushort_as_half(sbits));
+        float l[8];
+        levels8<BITS>(c, l);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (first) {
+                acc[j] = __fmul_rn(s, l[j]);
+            } else if constexpr (BITS <= 12) {
+                acc[j] = __fmaf_rn(s, l[j], acc[j]);
+            } else {
+                acc[j] = __fadd_rn(acc[j], __fmul_rn(s, l[j]));
+            }
+        }
+    }
+}
+
+// BOUT == 0: no requantisation (sum only).  MANY: W may exceed 8 (ranks are
+// then taken in groups of 8; the kernel gets a larger register budget).
+template <int BIN, int BOUT, bool SR, bool MANY>
+__global__ void __launch_bounds__(kThreads, (MANY || BIN >= 12 || BOUT >= 12) ? 1 : 2) decode_kernel(const DecArgs a)
 {
     constexpr int kGroup = 8;   // ranks whose loads are issued together
     __shared__ float red[2][kWarps];
@@ -32,24 +71,37 @@ __global__ void __launch_bounds__(kThreads, (BIN >= 12 || BOUT >= 12) ? 1 : 2) d
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
         if (valid > 0) {
-            for (int w0 = 0; w0 < W; w0 += kGroup) {
+            // ranks 0..7: all loads first, then the rank-ordered accumulation
+            {
                 Packed<BIN> c[kGroup];
-                float s[kGroup];
+                unsigned short sh[kGroup];
 #pragma unroll
                 for (int k = 0; k < kGroup; ++k) {
-                    if (w0 + k < W) {
-                        c[k] = load_codes<BIN>(a.codes[w0 + k], piece);
-                        s[k] = __half2float(__ushort_as_half(__ldg(a.scales[w0 + k] + blk_in)));
+                    if (k < W) {
+                        c[k] = load_codes<BIN>(a.codes[k], piece);
+                        sh[k] = __ldg(a.scales[k] + blk_in);
                     }
                 }
 #pragma unroll
                 for (int k = 0; k < kGroup; ++k) {
-                    if (w0 + k < W) {
+                    if (k < W) accumulate_rank<BIN>(c[k], sh[k], k == 0, acc);
+                }
+            }
+            if constexpr (MANY) {
+#pragma unroll 1
+                for (int w0 = kGroup; w0 < W; w0 += kGroup) {
+                    Packed<BIN> c[kGroup];
+                    unsigned short sh[kGroup];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float d = __fmul_rn(s[k], level_of<BIN>(get_code<BIN>(c[k], j)));
-                            acc[j] = (w0 + k == 0) ? d : __fadd_rn(acc[j], d);
+                    for (int k = 0; k < kGroup; ++k) {
+                        if (w0 + k < W) {
+                            c[k] = load_codes<BIN>(a.codes[w0 + k], piece);
+                            sh[k] = __ldg(a.scales[w0 + k] + blk_in);
                         }
+                    }
+#pragma unroll
+                    for (int k = 0; k < kGroup; ++k) {
+                        if (w0 + k < W) accumulate_rank<BIN>(c[k], sh[k], false, acc);
                     }
                 }
             }
@@ -111,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, (BIN >= 12 || BOUT >= 12) ? 1 : 2) d
             }
             Packed<BOUT> c;
             float q[8];
-            quantize8<BOUT, (SR && BOUT > 1)>(v, s2, rw, c, q);
+            quantize8<BOUT, (SR && BOUT > 1)>(v, s2, scale_reciprocal(s2), rw, c, q);
 
             if (e0 < (a.nb_out << a.log2Bout)) store_codes<BOUT>(a.codes_out, piece, c);
             if (team.lane == 0 && blk < a.nb_out) a.scales_out[blk] = __half_as_ushort(sh);
@@ -119,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, (BIN >= 12 || BOUT >= 12) ? 1 : 2) d
             if (a.err2 != nullptr) {
                 float e[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) e[j] = __fsub_rn(v[j], __fmul_rn(s2, q[j]));
+                for (int j = 0; j < 8; ++j) e[j] = feedback<BOUT>(v[j], s2, q[j]);
                 if (valid == 8) {
                     st8_f32(a.err2 + e0, e);
                 } else {
@@ -131,39 +183,40 @@ __global__ void __launch_bounds__(kThreads, (BIN >= 12 || BOUT >= 12) ? 1 : 2) d
     }
 }
 
-template <int BIN, int BOUT, bool SR>
+template <int BIN, int BOUT, bool SR, bool MANY>
 static cudaError_t run_decode(const DecArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};
     const int64_t rows = (a.n + kRow - 1) / kRow;
-    const int grid = grid_size(decode_kernel<BIN, BOUT, SR>, cap, rows);
-    decode_kernel<BIN, BOUT, SR><<<grid, kThreads, 0, st>>>(a);
+    const int grid = grid_size(decode_kernel<BIN, BOUT, SR, MANY>, cap, rows);
+    decode_kernel<BIN, BOUT, SR, MANY><<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 
-template <int B>
+template <int B, bool MANY>
 static cudaError_t decode_same(const DecArgs& a, int bits_out, bool sr, cudaStream_t st)
 {
-    if (bits_out == 0) return run_decode<B, 0, false>(a, st);
+    if (bits_out == 0) return run_decode<B, 0, false, MANY>(a, st);
     if (bits_out != B) return cudaErrorNotSupported;
     if constexpr (B == 1) {
-        return run_decode<1, 1, false>(a, st);
+        return run_decode<1, 1, false, MANY>(a, st);
     } else {
-        return sr ? run_decode<B, B, true>(a, st) : run_decode<B, B, false>(a, st);
+        return sr ? run_decode<B, B, true, MANY>(a, st) : run_decode<B, B, false, MANY>(a, st);
     }
 }
 
-cudaError_t launch_decode(const DecArgs& a, int bits_in, int bits_out, bool sr, cudaStream_t st)
+template <bool MANY>
+static cudaError_t decode_dispatch(const DecArgs& a, int bits_in, int bits_out, bool sr, cudaStream_t st)
 {
     if (bits_in == 8 && bits_out == 4)   // two-level: 8-bit intra stage, 4-bit inter stage
-        return sr ? run_decode<8, 4, true>(a, st) : run_decode<8, 4, false>(a, st);
+        return sr ? run_decode<8, 4, true, MANY>(a, st) : run_decode<8, 4, false, MANY>(a, st);
     switch (bits_in) {
-    case 1: return decode_same<1>(a, bits_out, sr, st);
-    case 2: return decode_same<2>(a, bits_out, sr, st);
-    case 4: return decode_same<4>(a, bits_out, sr, st);
-    case 8: return decode_same<8>(a, bits_out, sr, st);
-    case 12: return decode_same<12>(a, bits_out, sr, st);
-    case 16: return decode_same<16>(a, bits_out, sr, st);
+    case 1: return decode_same<1, MANY>(a, bits_out, sr, st);
+    case 2: return decode_same<2, MANY>(a, bits_out, sr, st);
+    case 4: return decode_same<4, MANY>(a, bits_out, sr, st);
+    case 8: return decode_same<8, MANY>(a, bits_out, sr, st);
+    case 12: return decode_same<12, MANY>(a, bits_out, sr, st);
+    case 16: return decode_same<16, MANY>(a, bits_out, sr, st);
     default: return cudaErrorNotSupported;
     }
 }

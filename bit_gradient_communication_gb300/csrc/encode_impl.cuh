@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
         }
         Packed<BITS> c;
         float q[8];
-        quantize8<BITS, (SR && BITS > 1)>(v, s, rw, c, q);
+        quantize8<BITS, (SR && BITS > 1)>(v, s, scale_reciprocal(s), rw, c, q);
 
         if (e0 < padded) store_codes<BITS>(a.codes, piece, c);
         if (team.lane == 0 && blk < a.nb) a.scales[blk] = __half_as_ushort(sh);
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
         if constexpr (EF) {
             float e[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) e[j] = __fsub_rn(v[j], __fmul_rn(s, q[j]));
+            for (int j = 0; j < 8; ++j) e[j] = feedback<BITS>(v[j], s, q[j]);
             if (valid == 8) {
                 st8_f32(a.err + e0, e);
             } else {

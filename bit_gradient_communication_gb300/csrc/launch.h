@@ -50,7 +50,13 @@ inline cudaError_t launch_encode(const EncArgs& a, int dtype, int bits, bool sr,
     return dtype == 0 ? launch_encode_f32(a, bits, sr, st) : launch_encode_bf16(a, bits, sr, st);
 }
 // bits_out == 0: no requantisation.
-cudaError_t launch_decode(const DecArgs& a, int bits_in, int bits_out, bool sr, cudaStream_t st);
+cudaError_t launch_decode_few(const DecArgs& a, int bits_in, int bits_out, bool sr, cudaStream_t st);
+cudaError_t launch_decode_many(const DecArgs& a, int bits_in, int bits_out, bool sr, cudaStream_t st);
+inline cudaError_t launch_decode(const DecArgs& a, int bits_in, int bits_out, bool sr, cudaStream_t st)
+{
+    return a.W <= 8 ? launch_decode_few(a, bits_in, bits_out, sr, st)
+                    : launch_decode_many(a, bits_in, bits_out, sr, st);
+}
 
 // Host-side argument checks of the encoder / decoder entry points (no CUDA
 // calls); shared by the plain entry points and the bucket scheduler.

@@ -212,3 +212,28 @@ def test_empty_input_is_a_no_op():
     x = torch.empty(0, device="cuda")
     codes, scales = bc.quantize_pack(x, bc.QParams(4, 128))
     assert codes.numel() == 0 and scales.numel() == 0
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_decoder_extreme_scales(bits):
+    # fp16 scales 0, 2^-24 (smallest subnormal), largest subnormal, 2^-14,
+    # 1.0 and 65504 with random codes: the dequantise-accumulate must stay
+    # bit-exact at both ends of the fp16 range.
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(bits)
+    n, W, B = 4 * 4096 + 24, 8, 32
+    special = np.array([0x0000, 0x0001, 0x03FF, 0x0400, 0x3C00, 0x7BFF], dtype=np.uint16)
+    ins = []
+    for _ in range(W):
+        codes = rng.integers(0, 256, O.packed_bytes(n, bits, B), dtype=np.uint8)
+        scales = special[rng.integers(0, special.size, O.num_blocks(n, B))]
+        ins.append((codes, scales))
+    cin = [torch.from_numpy(c).cuda() for c, _ in ins]
+    sin = [torch.from_numpy(s.view(np.int16)).cuda() for _, s in ins]
+    pin = bc.QParams(bits, B)
+    sum_, co, so = bc.unpack_dequant_reduce_requant(cin, sin, n, pin, sum_out=True, p_out=pin)
+    s_ref, c_ref, sc_ref = O.unpack_dequant_reduce_requant([c for c, _ in ins], [s for _, s in ins], n,
+                                                           O.params(bits, B), True, None, O.params(bits, B))
+    assert np.array_equal(sum_.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert co.cpu().numpy().tobytes() == c_ref.tobytes()
+    assert np.array_equal(so.cpu().numpy().view(np.uint16), sc_ref)
