@@ -48,10 +48,36 @@ __device__ __forceinline__ void accumulate_rank(const Packed<BITS>& c, unsigned 
     }
 }
 
-// BOUT == 0: no requantisation (sum only).  MANY: W may exceed 8 (ranks are
-// then taken in groups of 8; the kernel gets a larger register budget).
+// The first (up to) 8 ranks' codes and fp16 scales of one thread's piece.
+template <int BIN>
+struct RowCodes {
+    Packed<BIN> c[8];
+    unsigned short s[8];
+};
+
+template <int BIN>
+__device__ __forceinline__ void load_row_codes(const DecArgs& a, int64_t row, RowCodes<BIN>& r)
+{
+    const int64_t e0 = row * kRow + (int64_t)threadIdx.x * kPiece;
+    if (e0 >= a.n) return;
+    const int64_t piece = e0 >> 3, blk_in = e0 >> a.log2Bin;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (k < a.W) {
+            r.c[k] = load_codes<BIN>(a.codes[k], piece);
+            r.s[k] = __ldg(a.scales[k] + blk_in);
+        }
+    }
+}
+
+// BOUT == 0: no requantisation (sum only).  MANY: W may exceed 8 (ranks 8..W-1
+// are taken in groups of 8 inside the row; the kernel gets a larger register
+// budget).  The row loop is software-pipelined: the next row's codes and
+// scales of ranks 0..7 are loaded while the current row is requantised, and
+// the stage-2 error of the current row while its ranks are summed.
 template <int BIN, int BOUT, bool SR, bool MANY>
-__global__ void __launch_bounds__(kThreads, (MANY || BIN >= 12 || BOUT >= 12) ? 1 : 2) decode_kernel(const DecArgs a)
+__global__ void __launch_bounds__(kThreads, (MANY || BIN >= 12 || BOUT >= 12 || (SR && BIN >= 8)) ? 1 : 2)
+decode_kernel(const DecArgs a)
 {
     constexpr int kGroup = 8;   // ranks whose loads are issued together
     __shared__ float red[2][kWarps];
@@ -60,6 +86,8 @@ __global__ void __launch_bounds__(kThreads, (MANY || BIN >= 12 || BOUT >= 12) ? 
     const int W = a.W;
     int parity = 0;
 
+    RowCodes<BIN> cur;
+    if ((int64_t)blockIdx.x < rows) load_row_codes<BIN>(a, blockIdx.x, cur);
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
         const int64_t e0 = row * kRow + (int64_t)threadIdx.x * kPiece;
         const int64_t piece = e0 >> 3;
@@ -67,25 +95,26 @@ __global__ void __launch_bounds__(kThreads, (MANY || BIN >= 12 || BOUT >= 12) ? 
         const int valid = rem <= 0 ? 0 : (rem >= 8 ? 8 : (int)rem);
         const int64_t blk_in = e0 >> a.log2Bin;
 
+        // stage-2 error of this row: in flight while the ranks are summed
+        float e2[8];
+        if constexpr (BOUT != 0) {
+            if (a.err2 != nullptr) {
+                if (valid == 8) {
+                    ld8_f32(a.err2 + e0, e2);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) e2[j] = (j < valid) ? a.err2[e0 + j] : 0.0f;
+                }
+            }
+        }
+
         float acc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
         if (valid > 0) {
-            // ranks 0..7: all loads first, then the rank-ordered accumulation
-            {
-                Packed<BIN> c[kGroup];
-                unsigned short sh[kGroup];
 #pragma unroll
-                for (int k = 0; k < kGroup; ++k) {
-                    if (k < W) {
-                        c[k] = load_codes<BIN>(a.codes[k], piece);
-                        sh[k] = __ldg(a.scales[k] + blk_in);
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < kGroup; ++k) {
-                    if (k < W) accumulate_rank<BIN>(c[k], sh[k], k == 0, acc);
-                }
+            for (int k = 0; k < kGroup; ++k) {
+                if (k < W) accumulate_rank<BIN>(cur.c[k], cur.s[k], k == 0, acc);
             }
             if constexpr (MANY) {
 #pragma unroll 1
@@ -106,6 +135,8 @@ __global__ void __launch_bounds__(kThreads, (MANY || BIN >= 12 || BOUT >= 12) ? 
                 }
             }
         }
+        // prefetch: the next row's codes overlap this row's requantisation
+        if (row + gridDim.x < rows) load_row_codes<BIN>(a, row + gridDim.x, cur);
 
         if (a.sum_out != nullptr) {
             if (valid == 8) {
@@ -120,15 +151,8 @@ __global__ void __launch_bounds__(kThreads, (MANY || BIN >= 12 || BOUT >= 12) ? 
             const Team team = make_team(a.log2Bout);
             float v[8];
             if (a.err2 != nullptr) {
-                if (valid == 8) {
-                    float e[8];
-                    ld8_f32(a.err2 + e0, e);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) v[j] = __fadd_rn(acc[j], e[j]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) v[j] = (j < valid) ? __fadd_rn(acc[j], a.err2[e0 + j]) : 0.0f;
-                }
+                for (int j = 0; j < 8; ++j) v[j] = (j < valid) ? __fadd_rn(acc[j], e2[j]) : 0.0f;
             } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[j] = (j < valid) ? acc[j] : 0.0f;

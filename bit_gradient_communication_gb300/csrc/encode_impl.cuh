@@ -11,7 +11,51 @@
 
 namespace bitscom {
 
-// IN: 0 = fp32, 1 = bf16.
+// One thread's raw inputs for one row: the gradient bits as loaded (fp32, or
+// 8 bf16 in a uint4) and the error buffer.  Kept raw so that the loads of the
+// next row can be in flight while the current row is computed.
+template <int IN, bool EF>
+struct RowIn {
+    float g[IN == 0 ? 8 : 1];
+    uint4 gb;
+    float e[EF ? 8 : 1];
+};
+
+template <int IN, bool EF>
+__device__ __forceinline__ void load_row(const EncArgs& a, int64_t row, RowIn<IN, EF>& r)
+{
+    const int64_t e0 = row * kRow + (int64_t)threadIdx.x * kPiece;
+    if ((row + 1) * kRow <= a.n) {
+        if constexpr (IN == 0) {
+            ld8_f32_stream(static_cast<const float*>(a.x) + e0, r.g);
+        } else {
+            r.gb = ld16_stream(static_cast<const uint16_t*>(a.x) + e0);
+        }
+        if constexpr (EF) ld8_f32(a.err + e0, r.e);
+        return;
+    }
+    // the last, partial row: element loads, zero fill past n
+    const int64_t rem = a.n - e0;
+    const int valid = rem <= 0 ? 0 : (rem >= 8 ? 8 : (int)rem);
+    uint32_t hb[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const bool in = j < valid;
+        if constexpr (IN == 0) {
+            r.g[j] = in ? static_cast<const float*>(a.x)[e0 + j] : 0.0f;
+        } else {
+            hb[j] = in ? (uint32_t)static_cast<const uint16_t*>(a.x)[e0 + j] : 0u;
+        }
+        if constexpr (EF) r.e[j] = in ? a.err[e0 + j] : 0.0f;
+    }
+    if constexpr (IN == 1) {
+        r.gb = make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16),
+                          hb[6] | (hb[7] << 16));
+    }
+}
+
+// IN: 0 = fp32, 1 = bf16.  The row loop is software-pipelined: the loads of
+// row r + gridDim.x are issued before row r is computed.
 template <int IN, int BITS, bool EF, bool SR>
 __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
 {
@@ -24,41 +68,26 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
     const uint32_t shift = (uint32_t)(a.index_offset & 3u);
     int parity = 0;
 
+    RowIn<IN, EF> cur;
+    if ((int64_t)blockIdx.x < rows) load_row<IN, EF>(a, blockIdx.x, cur);
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
         const int64_t e0 = row * kRow + (int64_t)threadIdx.x * kPiece;
         const int64_t piece = e0 >> 3;
-        const bool full_row = (row + 1) * kRow <= n;
-        int valid = 8;
+        const int64_t rem = n - e0;
+        const int valid = rem <= 0 ? 0 : (rem >= 8 ? 8 : (int)rem);
         float v[8];
-        if (full_row) {
-            if constexpr (IN == 0) {
-                ld8_f32_stream(static_cast<const float*>(a.x) + e0, v);
-            } else {
-                bf16x8_to_f32(ld16_stream(static_cast<const uint16_t*>(a.x) + e0), v);
-            }
-            if constexpr (EF) {
-                float e[8];
-                ld8_f32(a.err + e0, e);
+        if constexpr (IN == 0) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) v[j] = __fadd_rn(v[j], e[j]);
-            }
+            for (int j = 0; j < 8; ++j) v[j] = cur.g[j];
         } else {
-            const int64_t rem = n - e0;
-            valid = rem <= 0 ? 0 : (rem >= 8 ? 8 : (int)rem);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float g = 0.0f;
-                if (j < valid) {
-                    if constexpr (IN == 0) {
-                        g = static_cast<const float*>(a.x)[e0 + j];
-                    } else {
-                        g = __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[e0 + j] << 16);
-                    }
-                    if constexpr (EF) g = __fadd_rn(g, a.err[e0 + j]);
-                }
-                v[j] = g;
-            }
+            bf16x8_to_f32(cur.gb, v);
         }
+        if constexpr (EF) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __fadd_rn(v[j], cur.e[j]);
+        }
+        // prefetch: the next row's loads overlap this row's arithmetic
+        if (row + gridDim.x < rows) load_row<IN, EF>(a, row + gridDim.x, cur);
 
         // block statistic: absmax (b >= 2) or tree sum of |v| (b = 1)
         float stat;
