@@ -12,6 +12,7 @@ Parity status of each function (details in the tests):
                                          unbiasedness, numpy packbits)
   unpack_dequant_reduce_requant          pinned (W=1 == dequant, hand sums,
                                          telescoping error-feedback bound)
+  unpack_dequant, f32_to_bf16            pinned (W=1 decoder sums, torch bf16 cast)
   tail blocks (n mod B != 0), 1-bit SR   parity unpinned (readings only)
 """
 from __future__ import annotations
@@ -88,6 +89,10 @@ def lib():
             L.orc_unpack_dequant_reduce_requant.argtypes = [vp, vp, i32, i64, P, vp, vp, P, vp, vp]
             L.orc_roundtrip.restype = ctypes.c_int
             L.orc_roundtrip.argtypes = [vp, i32, i64, vp, P, vp, vp, vp]
+            L.orc_unpack_dequant.restype = ctypes.c_int
+            L.orc_unpack_dequant.argtypes = [vp, vp, i64, P, ctypes.c_float, i32, vp]
+            L.orc_f32_to_bf16.restype = ctypes.c_uint16
+            L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
             L.orc_num_blocks.restype = i64
             L.orc_num_blocks.argtypes = [i64, i32]
             L.orc_packed_bytes.restype = i64
@@ -183,6 +188,24 @@ def unpack_dequant_reduce_requant(codes_in, scales_in, n: int, p_in: Params,
     if rc:
         raise ValueError("oracle rejected the arguments")
     return sum_out, codes_out, scales_out
+
+
+def unpack_dequant(codes, scales, n: int, p: Params, mul: float = 1.0, out_dtype: int = F32):
+    """All-gather-side decode: fl(fl(s*q) * mul) as fp32, or bf16 bit patterns."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    out = np.zeros(n, dtype=np.float32 if out_dtype == F32 else np.uint16)
+    rc = lib().orc_unpack_dequant(_ptr(codes), _ptr(scales), n, ctypes.byref(p), ctypes.c_float(mul),
+                                  out_dtype, _ptr(out))
+    if rc:
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    L = lib()
+    return np.array([L.orc_f32_to_bf16(float(v)) for v in x], dtype=np.uint16)
 
 
 def roundtrip(x: np.ndarray, p: Params, err: np.ndarray | None = None):

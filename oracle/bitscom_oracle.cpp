@@ -88,6 +88,19 @@ float orc_f16_to_f32(uint16_t h)
 
 float orc_bf16_to_f32(uint16_t b) { return float_of((uint32_t)b << 16); }
 
+/* binary32 -> bfloat16, round to nearest even: keep the top 16 bits and
+ * round on the 16 dropped ones (ties to an even kept part); a carry out of the
+ * mantissa moves into the exponent, so the largest finite values overflow to
+ * infinity exactly as IEEE rounding does.  NaN stays a quiet NaN. */
+uint16_t orc_f32_to_bf16(float x)
+{
+    uint32_t u = bits_of(x);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x7FFFFFu)) return (uint16_t)((u >> 16) | 0x40u);
+    uint32_t kept = u >> 16, dropped = u & 0xFFFFu;
+    if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u))) kept += 1;
+    return (uint16_t)kept;
+}
+
 void orc_f32_to_f16_many(const float* x, uint16_t* out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_f16(x[i]);
@@ -358,6 +371,28 @@ int orc_unpack_dequant_reduce_requant(const uint8_t* const* codes_in,
         quantize_stage(r, n, p_out, err2, codes_out, scales_out);      /* e2' = v2 - s2*q2 */
     }
     delete[] r;
+    return 0;
+}
+
+/* The all-gather side of the low-bit all-reduce: after the all-gather every
+ * rank holds the requantised chunks of all ranks (bitscom README,
+ * "Implemented Features": all-to-all -> local reduce -> all-gather) and
+ * decodes them into its gradient.  The reduce is a SUM; averaging is the
+ * caller's multiplier (reading: mul = 1/W gives the mean). */
+int orc_unpack_dequant(const uint8_t* codes, const uint16_t* scales, int64_t n,
+                       const orc_params* p, float mul, int32_t out_dtype, void* out)
+{
+    if (!valid_params(p) || n < 0 || (out_dtype != 0 && out_dtype != 1)) return 1;
+    if (n == 0) return 0;
+    if (!codes || !scales || !out) return 1;
+    for (int64_t i = 0; i < n; ++i) {
+        float s = orc_f16_to_f32(scales[i / p->block]);
+        int32_t q = code_to_q(get_code(codes, i, p->bits), p->bits);
+        float d = s * (float)q;
+        float y = d * mul;
+        if (out_dtype == 0) ((float*)out)[i] = y;
+        else ((uint16_t*)out)[i] = orc_f32_to_bf16(y);
+    }
     return 0;
 }
 

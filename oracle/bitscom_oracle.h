@@ -66,6 +66,12 @@ int orc_unpack_dequant_reduce_requant(const uint8_t* const* codes_in,
 int orc_roundtrip(const void* x, int32_t dtype, int64_t n, float* err,
                   const orc_params* p, uint8_t* codes, uint16_t* scales, float* deq_out);
 
+/* All-gather-side decode: out[i] = fl(fl(s*q) * mul) for i < n, written as
+ * fp32 (out_dtype 0) or bf16 bits (out_dtype 1, round to nearest even). */
+int orc_unpack_dequant(const uint8_t* codes, const uint16_t* scales, int64_t n,
+                       const orc_params* p, float mul, int32_t out_dtype, void* out);
+uint16_t orc_f32_to_bf16(float x);
+
 /* Sizes. */
 int64_t orc_num_blocks(int64_t n, int32_t block);
 int64_t orc_packed_bytes(int64_t n, int32_t bits, int32_t block);

@@ -34,6 +34,8 @@ MUTANTS = {
     "left_fold_mean": ("return tree_sum(a, n / 2) + tree_sum(a + n / 2, n / 2);",
                        "float acc = 0.0f; for (int64_t i = 0; i < n; ++i) acc += a[i]; return acc;"),
     "stage2_ef_dropped": ("r[i] = r[i] + err2[i];", "r[i] = r[i];"),
+    "bf16_truncates": ("if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u))) kept += 1;", ";"),
+    "mul_inside_product": ("float y = d * mul;", "float y = s * ((float)q * mul);"),
     "fma_in_feedback": ("float d = s * (float)q;          /* separate roundings, no FMA */\n                err_out[e] = val - d;",
                         "err_out[e] = fmaf(-s, (float)q, val);"),
 }

@@ -504,3 +504,39 @@ def test_requant_equals_encoder_on_the_sum(orc, bin_, bout, Bin, Bout):
     # quantize_pack adds its err input (zeros) to v2: identical values
     assert co.tobytes() == c_ref.tobytes() and (so == s_ref).all()
     np.testing.assert_array_equal(e2.view(np.uint32), e_ref.view(np.uint32))
+
+
+# ---- all-gather-side decode ------------------------------------------------
+
+def test_f32_to_bf16_matches_torch(orc):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(8)
+    u = np.concatenate([rng.integers(0, 2 ** 32, 200_000, dtype=np.uint64).astype(np.uint32),
+                        np.arange(0x7F7F0000, 0x7F800000, 7, dtype=np.uint32),     # overflow boundary
+                        np.arange(0x00000000, 0x00030000, 3, dtype=np.uint32),     # subnormals
+                        (np.arange(0, 65536, dtype=np.uint32) << 16) | 0x8000])   # exact ties
+    x = u.view(np.float32)
+    x = x[~np.isnan(x)]
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    L = orc.lib()
+    got = np.fromiter((L.orc_f32_to_bf16(float(v)) for v in x), dtype=np.uint16, count=x.size)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [hex(int(x.view(np.uint32)[i])) for i in bad[:5]]
+
+
+@pytest.mark.parametrize("bits", [1, 2, 4, 8, 12, 16])
+def test_unpack_dequant_equals_single_rank_sum(orc, bits):
+    # With mul = 1 and fp32 output the all-gather-side decode is the W=1
+    # decoder's sum; with mul = 1/4 every value is that sum times 2^-2 exactly.
+    rng = np.random.default_rng(bits)
+    n = 3000
+    x = rng.standard_normal(n).astype(np.float32)
+    p = orc.params(bits, 128)
+    c, s = orc.quantize_pack(x, p)
+    ref, _, _ = orc.unpack_dequant_reduce_requant([c], [s], n, p)
+    np.testing.assert_array_equal(orc.unpack_dequant(c, s, n, p).view(np.uint32), ref.view(np.uint32))
+    np.testing.assert_array_equal(orc.unpack_dequant(c, s, n, p, mul=0.25), ref * np.float32(0.25))
+    bf = orc.unpack_dequant(c, s, n, p, mul=0.25, out_dtype=orc.BF16)
+    torch = pytest.importorskip("torch")
+    exp = torch.from_numpy(ref * np.float32(0.25)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(bf, exp)
