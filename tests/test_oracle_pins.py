@@ -536,6 +536,10 @@ def test_unpack_dequant_equals_single_rank_sum(orc, bits):
     ref, _, _ = orc.unpack_dequant_reduce_requant([c], [s], n, p)
     np.testing.assert_array_equal(orc.unpack_dequant(c, s, n, p).view(np.uint32), ref.view(np.uint32))
     np.testing.assert_array_equal(orc.unpack_dequant(c, s, n, p, mul=0.25), ref * np.float32(0.25))
+    # a multiplier that rounds: the product s*q is rounded first, then scaled
+    third = np.float32(1.0 / 3.0)
+    np.testing.assert_array_equal(orc.unpack_dequant(c, s, n, p, mul=float(third)).view(np.uint32),
+                                  (ref * third).astype(np.float32).view(np.uint32))
     bf = orc.unpack_dequant(c, s, n, p, mul=0.25, out_dtype=orc.BF16)
     torch = pytest.importorskip("torch")
     exp = torch.from_numpy(ref * np.float32(0.25)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
