@@ -11,6 +11,7 @@ The names follow the C ABI:
   unpack_dequant_reduce_requant  decoder of one chunk between the all-to-all
                                  and the all-gather (rank-ordered fp32 sum,
                                  stage-2 error feedback, requantise + repack)
+  unpack_dequant                 all-gather-side decode into fp32 / bf16
   roundtrip                      quantise then dequantise
   Scheduler                      fusion buckets on CUDA streams
 """
@@ -97,6 +98,8 @@ def lib():
             L.bitscom_unpack_dequant_reduce_requant.argtypes = [vp, vp, i32, i64, P, vp, vp, P, vp, vp, vp]
             L.bitscom_roundtrip.restype = st
             L.bitscom_roundtrip.argtypes = [vp, st, i64, vp, P, vp, vp, vp, vp]
+            L.bitscom_unpack_dequant.restype = st
+            L.bitscom_unpack_dequant.argtypes = [vp, vp, i64, P, ctypes.c_float, st, vp, vp]
             L.bitscom_roundtrip_noalloc.restype = st
             L.bitscom_roundtrip_noalloc.argtypes = [vp, st, i64, vp, P, vp, vp]
             L.bitscom_roundtrip_noalloc_max_elements.restype = i64
@@ -223,6 +226,19 @@ def unpack_dequant_reduce_requant(codes_in: Sequence, scales_in: Sequence, n: in
         _dev_ptr(scales_out, "scales_out") if p_out is not None else None, _stream(stream)),
         "bitscom_unpack_dequant_reduce_requant")
     return sum_out, codes_out, scales_out
+
+
+def unpack_dequant(codes, scales, n: int, p: QParams, mul: float = 1.0, out=None, out_dtype=None,
+                   stream=None):
+    """All-gather-side decode: out = fl(fl(s*q) * mul) as fp32 or bf16 (out's
+    dtype, or out_dtype when out is None; fp32 by default)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(n, dtype=out_dtype or torch.float32, device=codes.device)
+    _check(lib().bitscom_unpack_dequant(_dev_ptr(codes, "codes"), _dev_ptr(scales, "scales"), n,
+                                        ctypes.byref(p.c()), ctypes.c_float(mul), _dtype_code(out),
+                                        _dev_ptr(out, "out"), _stream(stream)), "bitscom_unpack_dequant")
+    return out
 
 
 def roundtrip(x, p: QParams, err=None, codes_tmp=None, scales_tmp=None, deq_out=None, stream=None):

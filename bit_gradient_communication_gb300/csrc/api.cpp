@@ -181,6 +181,27 @@ bitscom_status bitscom_unpack_dequant_reduce_requant(
                                               static_cast<cudaStream_t>(cuda_stream)));
 }
 
+bitscom_status bitscom_unpack_dequant(const void* codes, const uint16_t* scales, int64_t n,
+                                     const bitscom_qparams* p, float mul, bitscom_dtype out_dt,
+                                     void* out, void* cuda_stream)
+{
+    if (!valid_params(p) || n < 0 || (out_dt != BITSCOM_F32 && out_dt != BITSCOM_BF16)) return BITSCOM_EINVAL;
+    if (n == 0) return BITSCOM_OK;
+    if (!codes || !scales || !out) return BITSCOM_EINVAL;
+    if (!aligned(codes, code_align(p->bits)) || !aligned(scales, 2) ||
+        !aligned(out, out_dt == BITSCOM_F32 ? 32 : 16))
+        return BITSCOM_EALIGN;
+    bitscom::DqArgs a;
+    a.codes = static_cast<const uint8_t*>(codes);
+    a.scales = scales;
+    a.n = n;
+    a.log2B = log2_block(p->block);
+    a.mul = mul;
+    a.out = out;
+    return cuda_status(bitscom::launch_dequant(a, p->bits, out_dt == BITSCOM_F32 ? 0 : 1,
+                                               static_cast<cudaStream_t>(cuda_stream)));
+}
+
 bitscom_status bitscom_roundtrip(const void* x, bitscom_dtype dt, int64_t n, float* err,
                                  const bitscom_qparams* p, void* codes_tmp,
                                  uint16_t* scales_tmp, float* deq_out, void* cuda_stream)

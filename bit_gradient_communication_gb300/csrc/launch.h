@@ -41,6 +41,15 @@ struct DecArgs {
     uint64_t index_offset;
 };
 
+struct DqArgs {
+    const uint8_t* codes;
+    const uint16_t* scales;
+    int64_t n;
+    int log2B;
+    float mul;
+    void* out;              // fp32 or bf16 [n]
+};
+
 // Return cudaErrorNotSupported for a combination without a kernel.
 cudaError_t launch_encode_f32(const EncArgs& a, int bits, bool sr, cudaStream_t st);
 cudaError_t launch_encode_bf16(const EncArgs& a, int bits, bool sr, cudaStream_t st);
@@ -57,6 +66,9 @@ inline cudaError_t launch_decode(const DecArgs& a, int bits_in, int bits_out, bo
     return a.W <= 8 ? launch_decode_few(a, bits_in, bits_out, sr, st)
                     : launch_decode_many(a, bits_in, bits_out, sr, st);
 }
+
+// out_dtype 0 = fp32, 1 = bf16.
+cudaError_t launch_dequant(const DqArgs& a, int bits, int out_dtype, cudaStream_t st);
 
 // Host-side argument checks of the encoder / decoder entry points (no CUDA
 // calls); shared by the plain entry points and the bucket scheduler.

@@ -140,6 +140,20 @@ bitscom_status bitscom_unpack_dequant_reduce_requant(
     void* codes_out, uint16_t* scales_out, void* cuda_stream);
 
 /*
+ * All-gather-side decode: after the all-gather of the low-bit all-reduce every
+ * rank holds all ranks' requantised chunks (bitscom README, "Implemented
+ * Features": all-to-all -> local reduce -> all-gather) and decodes them into
+ * its gradient: out[i] = fl(fl(s*q) * mul), written as fp32 (out 32-byte
+ * aligned) or bf16 (round to nearest even, out 16-byte aligned).  The reduce
+ * is a SUM; mul = 1/W turns it into the mean.
+ *   codes, scales   one stream of packed codes / fp16 scales of n elements for
+ *                   p (alignment as the encoder's outputs).
+ */
+bitscom_status bitscom_unpack_dequant(const void* codes, const uint16_t* scales, int64_t n,
+                                      const bitscom_qparams* p, float mul, bitscom_dtype out_dt,
+                                      void* out, void* cuda_stream);
+
+/*
  * Quantise then dequantise (the simulate_quantization mode of "Implemented
  * Features"): the encoder into caller scratch codes_tmp / scales_tmp, then the
  * single-rank decoder into deq_out.  deq_out may alias x when dt == F32.

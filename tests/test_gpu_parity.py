@@ -237,3 +237,23 @@ def test_decoder_extreme_scales(bits):
     assert np.array_equal(sum_.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
     assert co.cpu().numpy().tobytes() == c_ref.tobytes()
     assert np.array_equal(so.cpu().numpy().view(np.uint16), sc_ref)
+
+
+@pytest.mark.parametrize("bits", BITS)
+@pytest.mark.parametrize("block", [8, 128, 4096])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_allgather_decode_matches_oracle(bits, block, out):
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(bits * 31 + block)
+    for n, mul in ((13, 1.0), (3 * 4096 + 40, 0.125), (5 * 4096 + 8, float(np.float32(1 / 3)))):
+        codes, scales = _random_codes(rng, n, bits, block)
+        cg = Guarded(torch, codes.size, fill=codes)
+        sg = Guarded(torch, 2 * scales.size, fill=scales)
+        og = Guarded(torch, (4 if out == "f32" else 2) * n)
+        dst = og.view(torch.float32 if out == "f32" else torch.bfloat16)
+        bc.unpack_dequant(cg.view(torch.uint8), sg.view(torch.int16), n, bc.QParams(bits, block), mul, out=dst)
+        torch.cuda.synchronize()
+        assert og.guards_intact()
+        ref = O.unpack_dequant(codes, scales, n, O.params(bits, block), mul, O.F32 if out == "f32" else O.BF16)
+        got = og.host(np.uint32 if out == "f32" else np.uint16)
+        assert np.array_equal(got, ref.view(np.uint32 if out == "f32" else np.uint16)), f"n={n} mul={mul}"

@@ -148,3 +148,29 @@ def test_host_wait_times_out_then_completes():
     assert ei.value.status == 5
     sched.wait(timeout_s=60.0)
     sched.close()
+
+
+def test_allreduce_then_allgather_decode_matches_oracle():
+    # The whole low-bit all-reduce: encoders, chunk decoders, and every rank's
+    # decode of the all-gathered requantised codes into its mean gradient (bf16).
+    _, bc = need_gpu()
+    W, n = 4, 20 * 4096 + 64
+    sched = bc.Scheduler(n_streams=2, bucket_bytes=64 * 1024)
+    xs = [_x(n, 40 + w, "bf16") for w in range(W)]
+    errs = [torch.zeros(n, device="cuda") for _ in range(W)]
+    p1 = [bc.QParams(4, 128, bc.RTN) for _ in range(W)]
+    p2 = bc.QParams(4, 128, bc.RTN, philox_stream=1)
+    codes, scales = zip(*[bc.alloc_codes(n, p1[0]) for _ in range(W)])
+    err2 = torch.zeros(n, device="cuda")
+    co, so = bc.alloc_codes(n, p2)
+    sched.allreduce(xs, p1, codes, scales, errs, p2, err2, co, so)
+    mean = bc.unpack_dequant(co, so, n, p2, mul=1.0 / W, out_dtype=torch.bfloat16)
+    sched.wait()
+    torch.cuda.synchronize()
+    h_err = [np.zeros(n, np.float32) for _ in range(W)]
+    _, _, c_ref, s_ref = _oracle_allreduce([_host_bits(x) for x in xs], n, W,
+                                           [O.params(4, 128) for _ in range(W)],
+                                           O.params(4, 128, philox_stream=1), h_err, np.zeros(n, np.float32))
+    ref = O.unpack_dequant(c_ref, s_ref, n, O.params(4, 128), float(np.float32(1.0 / W)), O.BF16)
+    assert np.array_equal(_host_bits(mean), ref)
+    sched.close()
