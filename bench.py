@@ -499,6 +499,18 @@ def run_workload(args):
         algo = wl.n * (12 + 0.5 + 2 / wl.block)
         extra = {"l2": "flushed between timed iterations (256 MB write)", "per_bits": per_bits,
                  "value_is": "4-bit"}
+    elif args.workload == "allgather_decode_gpt1p3b":
+        # every rank's decode of the all-gathered 4-bit codes into its bf16 mean gradient
+        x = synth.gradients(wl.kind, wl.n, wl.seed, dtype=dt, **wl.params)
+        p = bc.QParams(wl.bits, wl.block)
+        codes, scales = bc.quantize_pack(x, p)
+        out = torch.empty(wl.n, dtype=torch.bfloat16, device="cuda")
+        step = lambda: bc.unpack_dequant(codes, scales, wl.n, p, 1.0 / wl.ranks, out)
+        for _ in range(warm):
+            step()
+        t = _timed(torch, step, K)
+        algo = wl.n * (wl.bits / 8 + 2 / wl.block + 2)
+        extra = {"l2": "inputs larger than L2 (3.3 GB per step)", "output": "bf16", "mul": "1/8"}
     elif args.workload == "gpt6p7b_2bit_buckets":
         sched = bc.Scheduler(2, wl.bucket_bytes)
         x = synth.gradients(wl.kind, wl.n, wl.seed, dtype=dt, **wl.params)
