@@ -46,7 +46,12 @@ DEC_BYTES_PER_ELEM = W_RANKS * (BITS / 8 + 2 / BLOCK) + 4 + 4 + BITS / 8 + 2 / B
 # DRAM traffic per element measured by ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum over the captured launch / its elements), valid only
 # while the kernel sources hash to `src`.  Filled from profiles/.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/launches_allreduce_w8_gpt1p3b.md: one full-size step, 1.3e9 elements per
+    # encoder launch, 1.625e8 output elements per decoder launch
+    "encode": {"src": "8d39506f4bd3d9aa", "bytes_per_elem": (7.8118e9 + 5.8199e9) / 1.3e9},
+    "decode": {"src": "8d39506f4bd3d9aa", "bytes_per_elem": (1.3205e9 + 0.6842e9) / 1.625e8},
+}
 
 
 def kernel_src_hash() -> str:
@@ -237,7 +242,9 @@ def run_ours(args, rank, world, local_rank):
     dec_gbs = dec_bytes / dec_launch_s / 1e9
     src = kernel_src_hash()
     tr = NCU_TRAFFIC.get("encode")
-    traffic = tr["bytes_per_elem"] * n if tr and tr["src"] == src else None
+    traffic = round(tr["bytes_per_elem"] * n) if tr and tr["src"] == src else None
+    trd = NCU_TRAFFIC.get("decode")
+    dec_traffic = round(trd["bytes_per_elem"] * n / len(ar.chunks)) if trd and trd["src"] == src else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
@@ -257,7 +264,8 @@ def run_ours(args, rank, world, local_rank):
             "encode": {"gbs": round(enc_gbs, 1), "frac": round(enc_gbs / peak, 4),
                        "launch_ms": round(enc_launch_s * 1e3, 4), "bytes_per_elem": ENC_BYTES_PER_ELEM},
             "decode_w8": {"gbs": round(dec_gbs, 1), "frac": round(dec_gbs / peak, 4),
-                          "launch_ms": round(dec_launch_s * 1e3, 4), "bytes_per_elem": DEC_BYTES_PER_ELEM},
+                          "launch_ms": round(dec_launch_s * 1e3, 4), "bytes_per_elem": DEC_BYTES_PER_ELEM,
+                          "traffic": dec_traffic, "bytes_per_launch": dec_bytes},
         },
         "gpu_launches": K * (W + len(ar.chunks)),
         "clocks": clk,
