@@ -1,4 +1,5 @@
-// Decoder instantiations for W <= 8 ranks (the all-reduce of one node).
+// Decoder instantiations for 1..7 ranks (rank count read at run time).
+#define DEC_KW 0
 #include "decode_impl.cuh"
 
 namespace bitscom {

@@ -55,7 +55,7 @@ struct RowCodes {
     unsigned short s[8];
 };
 
-template <int BIN>
+template <int BIN, int KW>
 __device__ __forceinline__ void load_row_codes(const DecArgs& a, int64_t row, RowCodes<BIN>& r)
 {
     const int64_t e0 = row * kRow + (int64_t)threadIdx.x * kPiece;
@@ -63,7 +63,7 @@ __device__ __forceinline__ void load_row_codes(const DecArgs& a, int64_t row, Ro
     const int64_t piece = e0 >> 3, blk_in = e0 >> a.log2Bin;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        if (k < a.W) {
+        if (KW == 8 || k < a.W) {
             r.c[k] = load_codes<BIN>(a.codes[k], piece);
             r.s[k] = __ldg(a.scales[k] + blk_in);
         }
@@ -75,7 +75,9 @@ __device__ __forceinline__ void load_row_codes(const DecArgs& a, int64_t row, Ro
 // budget).  The row loop is software-pipelined: the next row's codes and
 // scales of ranks 0..7 are loaded while the current row is requantised, and
 // the stage-2 error of the current row while its ranks are summed.
-template <int BIN, int BOUT, bool SR, bool MANY>
+// KW == 8: exactly eight ranks, known at compile time (the all-reduce of one
+// eight-GPU node); KW == 0: the rank count is read from the arguments.
+template <int BIN, int BOUT, bool SR, bool MANY, int KW>
 __global__ void __launch_bounds__(kThreads, (MANY || BIN >= 12 || BOUT >= 12 || (SR && BIN >= 8)) ? 1 : 2)
 decode_kernel(const DecArgs a)
 {
@@ -83,11 +85,11 @@ decode_kernel(const DecArgs a)
     __shared__ float red[2][kWarps];
     const int64_t n = a.n;
     const int64_t rows = (n + kRow - 1) / kRow;
-    const int W = a.W;
+    const int W = KW == 8 ? 8 : a.W;
     int parity = 0;
 
     RowCodes<BIN> cur;
-    if ((int64_t)blockIdx.x < rows) load_row_codes<BIN>(a, blockIdx.x, cur);
+    if ((int64_t)blockIdx.x < rows) load_row_codes<BIN, KW>(a, blockIdx.x, cur);
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
         const int64_t e0 = row * kRow + (int64_t)threadIdx.x * kPiece;
         const int64_t piece = e0 >> 3;
@@ -136,7 +138,7 @@ decode_kernel(const DecArgs a)
             }
         }
         // prefetch: the next row's codes overlap this row's requantisation
-        if (row + gridDim.x < rows) load_row_codes<BIN>(a, row + gridDim.x, cur);
+        if (row + gridDim.x < rows) load_row_codes<BIN, KW>(a, row + gridDim.x, cur);
 
         if (a.sum_out != nullptr) {
             if (valid == 8) {
@@ -150,7 +152,10 @@ decode_kernel(const DecArgs a)
         if constexpr (BOUT != 0) {
             const Team team = make_team(a.log2Bout);
             float v[8];
-            if (a.err2 != nullptr) {
+            if (valid == 8) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = a.err2 != nullptr ? __fadd_rn(acc[j], e2[j]) : acc[j];
+            } else if (a.err2 != nullptr) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[j] = (j < valid) ? __fadd_rn(acc[j], e2[j]) : 0.0f;
             } else {
@@ -207,14 +212,22 @@ decode_kernel(const DecArgs a)
     }
 }
 
-template <int BIN, int BOUT, bool SR, bool MANY>
-static cudaError_t run_decode(const DecArgs& a, cudaStream_t st)
+template <int BIN, int BOUT, bool SR, bool MANY, int KW>
+static cudaError_t run_decode_kw(const DecArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};
     const int64_t rows = (a.n + kRow - 1) / kRow;
-    const int grid = grid_size(decode_kernel<BIN, BOUT, SR, MANY>, cap, rows);
-    decode_kernel<BIN, BOUT, SR, MANY><<<grid, kThreads, 0, st>>>(a);
+    const int grid = grid_size(decode_kernel<BIN, BOUT, SR, MANY, KW>, cap, rows);
+    decode_kernel<BIN, BOUT, SR, MANY, KW><<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
+}
+
+// DEC_KW selects the instantiations a translation unit compiles: 8 for
+// exactly eight ranks, 0 for a rank count read at run time.
+template <int BIN, int BOUT, bool SR, bool MANY>
+static cudaError_t run_decode(const DecArgs& a, cudaStream_t st)
+{
+    return run_decode_kw<BIN, BOUT, SR, MANY, (MANY ? 0 : DEC_KW)>(a, st);
 }
 
 template <int B, bool MANY>

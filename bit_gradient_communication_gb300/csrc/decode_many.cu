@@ -1,4 +1,5 @@
 // Decoder instantiations for W > 8 ranks (groups of 8 ranks per pass).
+#define DEC_KW 0
 #include "decode_impl.cuh"
 
 namespace bitscom {

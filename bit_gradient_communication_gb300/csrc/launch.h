@@ -60,11 +60,13 @@ inline cudaError_t launch_encode(const EncArgs& a, int dtype, int bits, bool sr,
 }
 // bits_out == 0: no requantisation.
 cudaError_t launch_decode_few(const DecArgs& a, int bits_in, int bits_out, bool sr, cudaStream_t st);
+cudaError_t launch_decode_w8(const DecArgs& a, int bits_in, int bits_out, bool sr, cudaStream_t st);
 cudaError_t launch_decode_many(const DecArgs& a, int bits_in, int bits_out, bool sr, cudaStream_t st);
 inline cudaError_t launch_decode(const DecArgs& a, int bits_in, int bits_out, bool sr, cudaStream_t st)
 {
-    return a.W <= 8 ? launch_decode_few(a, bits_in, bits_out, sr, st)
-                    : launch_decode_many(a, bits_in, bits_out, sr, st);
+    if (a.W == 8) return launch_decode_w8(a, bits_in, bits_out, sr, st);
+    return a.W < 8 ? launch_decode_few(a, bits_in, bits_out, sr, st)
+                   : launch_decode_many(a, bits_in, bits_out, sr, st);
 }
 
 // out_dtype 0 = fp32, 1 = bf16.
