@@ -13,6 +13,7 @@ Parity status of each function (details in the tests):
   unpack_dequant_reduce_requant          pinned (W=1 == dequant, hand sums,
                                          telescoping error-feedback bound)
   unpack_dequant, f32_to_bf16            pinned (W=1 decoder sums, torch bf16 cast)
+  fwht (Hadamard smoothing)              pinned (scipy Sylvester matrix, involution)
   tail blocks (n mod B != 0), 1-bit SR   parity unpinned (readings only)
 """
 from __future__ import annotations
@@ -58,11 +59,12 @@ def build(force: bool = False) -> str:
 class Params(ctypes.Structure):
     _fields_ = [("bits", ctypes.c_int32), ("block", ctypes.c_int32),
                 ("rounding", ctypes.c_int32), ("philox_stream", ctypes.c_uint32),
-                ("seed", ctypes.c_uint64), ("index_offset", ctypes.c_uint64)]
+                ("seed", ctypes.c_uint64), ("index_offset", ctypes.c_uint64),
+                ("hadamard", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
-def params(bits, block, rounding=RTN, seed=0, index_offset=0, philox_stream=0) -> Params:
-    return Params(bits, block, rounding, philox_stream, seed, index_offset)
+def params(bits, block, rounding=RTN, seed=0, index_offset=0, philox_stream=0, hadamard=0) -> Params:
+    return Params(bits, block, rounding, philox_stream, seed, index_offset, hadamard, 0)
 
 
 def lib():
@@ -93,6 +95,8 @@ def lib():
             L.orc_unpack_dequant.argtypes = [vp, vp, i64, P, ctypes.c_float, i32, vp]
             L.orc_f32_to_bf16.restype = ctypes.c_uint16
             L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+            L.orc_fwht.restype = ctypes.c_int
+            L.orc_fwht.argtypes = [vp, i64, i32]
             L.orc_num_blocks.restype = i64
             L.orc_num_blocks.argtypes = [i64, i32]
             L.orc_packed_bytes.restype = i64
@@ -208,7 +212,15 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return np.array([L.orc_f32_to_bf16(float(v)) for v in x], dtype=np.uint16)
 
 
+def fwht(x: np.ndarray, H: int) -> np.ndarray:
+    """Unnormalised Walsh-Hadamard transform of every H-block (a copy)."""
+    y = np.ascontiguousarray(x, dtype=np.float32).copy()
+    if lib().orc_fwht(_ptr(y), y.size, H):
+        raise ValueError("bad transform arguments")
+    return y
+
+
 def roundtrip(x: np.ndarray, p: Params, err: np.ndarray | None = None):
     codes, scales = quantize_pack(x, p, err)
-    deq, _, _ = unpack_dequant_reduce_requant([codes], [scales], x.size, p)
+    deq = unpack_dequant(codes, scales, x.size, p)
     return codes, scales, deq

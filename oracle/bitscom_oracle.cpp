@@ -152,10 +152,42 @@ uint32_t orc_random_word(uint64_t seed, uint32_t stream, uint64_t i)
 
 static int valid_bits(int b) { return b == 1 || b == 2 || b == 4 || b == 8 || b == 12 || b == 16; }
 static int valid_block(int B) { return B >= 8 && (B & (B - 1)) == 0; }
+/* Reading of the SDP4Bit README's "--hadamard-transform" (TLq-HS): a
+ * Walsh-Hadamard rotation of every H-element block before quantisation and
+ * its inverse after dequantisation; H is a power of two in [8, 256] dividing
+ * the quantisation block, and every stage of one all-reduce uses the same H. */
+static int valid_hadamard(int H, int B)
+{
+    return H == 0 || (H >= 8 && H <= 256 && (H & (H - 1)) == 0 && B % H == 0);
+}
+
 static int valid_params(const orc_params* p)
 {
     return p && valid_bits(p->bits) && valid_block(p->block) &&
-           (p->rounding == 0 || p->rounding == 1);
+           (p->rounding == 0 || p->rounding == 1) && valid_hadamard(p->hadamard, p->block);
+}
+
+/* Sylvester-ordered unnormalised Walsh-Hadamard transform of one block: stage
+ * h = 1, 2, 4, ... replaces (x[j], x[j+h]) by (x[j] + x[j+h], x[j] - x[j+h])
+ * for every j whose bit h is clear; each output is one fp32 operation, so the
+ * result does not depend on the order within a stage.  Applying it twice
+ * gives H times the input (up to rounding). */
+static void fwht_block(float* x, int H)
+{
+    for (int h = 1; h < H; h *= 2)
+        for (int i = 0; i < H; i += 2 * h)
+            for (int j = i; j < i + h; ++j) {
+                float a = x[j], b = x[j + h];
+                x[j] = a + b;
+                x[j + h] = a - b;
+            }
+}
+
+int orc_fwht(float* x, int64_t n, int32_t H)
+{
+    if (!x || H < 1 || (H & (H - 1)) != 0 || n < 0 || n % H != 0) return 1;
+    for (int64_t k = 0; k < n; k += H) fwht_block(x + k, H);
+    return 0;
 }
 
 int64_t orc_num_blocks(int64_t n, int32_t block) { return (n + block - 1) / block; }
@@ -321,11 +353,13 @@ int orc_quantize_pack(const void* x, int32_t dtype, int64_t n, float* err,
     if (!valid_params(p) || n < 0 || (dtype != 0 && dtype != 1)) return 1;
     if (n == 0) return 0;
     if (!x || !codes || !scales) return 1;
+    if (p->hadamard && n % p->hadamard != 0) return 1;
     float* v = new float[n];
-    for (int64_t i = 0; i < n; ++i) {
-        float g = (dtype == 0) ? ((const float*)x)[i] : orc_bf16_to_f32(((const uint16_t*)x)[i]);
-        v[i] = err ? (g + err[i]) : g;             /* a1: load + EF add (fp32 RN) */
-    }
+    for (int64_t i = 0; i < n; ++i)
+        v[i] = (dtype == 0) ? ((const float*)x)[i] : orc_bf16_to_f32(((const uint16_t*)x)[i]);
+    if (p->hadamard) orc_fwht(v, n, p->hadamard);  /* smoothing rotation of g */
+    if (err)
+        for (int64_t i = 0; i < n; ++i) v[i] = v[i] + err[i];   /* a1: EF add (fp32 RN) */
     quantize_stage(v, n, p, err, codes, scales);  /* a2-a6, e' written into err */
     delete[] v;
     return 0;
@@ -348,6 +382,8 @@ int orc_unpack_dequant_reduce_requant(const uint8_t* const* codes_in,
 {
     if (!valid_params(p_in) || W < 1 || n < 0) return 1;
     if (p_out && !valid_params(p_out)) return 1;
+    /* the rank sum and the requantisation stay in the transformed domain */
+    if (p_out && p_out->hadamard != p_in->hadamard) return 1;
     if (n == 0) return 0;
     if (!codes_in || !scales_in) return 1;
     for (int w = 0; w < W; ++w) if (!codes_in[w] || !scales_in[w]) return 1;
@@ -385,14 +421,25 @@ int orc_unpack_dequant(const uint8_t* codes, const uint16_t* scales, int64_t n,
     if (!valid_params(p) || n < 0 || (out_dtype != 0 && out_dtype != 1)) return 1;
     if (n == 0) return 0;
     if (!codes || !scales || !out) return 1;
+    const int H = p->hadamard;
+    if (H && n % H != 0) return 1;
+    float* d = new float[n];
     for (int64_t i = 0; i < n; ++i) {
         float s = orc_f16_to_f32(scales[i / p->block]);
         int32_t q = code_to_q(get_code(codes, i, p->bits), p->bits);
-        float d = s * (float)q;
-        float y = d * mul;
+        d[i] = s * (float)q;
+    }
+    if (H) {   /* inverse rotation: the same transform, then 1/H (exact) */
+        orc_fwht(d, n, H);
+        float inv = ldexpf(1.0f, -(int)log2((double)H));
+        for (int64_t i = 0; i < n; ++i) d[i] = d[i] * inv;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        float y = d[i] * mul;
         if (out_dtype == 0) ((float*)out)[i] = y;
         else ((uint16_t*)out)[i] = orc_f32_to_bf16(y);
     }
+    delete[] d;
     return 0;
 }
 
@@ -401,7 +448,5 @@ int orc_roundtrip(const void* x, int32_t dtype, int64_t n, float* err,
 {
     int rc = orc_quantize_pack(x, dtype, n, err, p, codes, scales);
     if (rc || n == 0) return rc;
-    const uint8_t* c[1] = { codes };
-    const uint16_t* s[1] = { scales };
-    return orc_unpack_dequant_reduce_requant(c, s, 1, n, p, deq_out, NULL, NULL, NULL, NULL);
+    return orc_unpack_dequant(codes, scales, n, p, 1.0f, 0, deq_out);
 }

@@ -34,6 +34,8 @@ typedef struct {
     uint32_t philox_stream;  /* third Philox counter word                 */
     uint64_t seed;           /* Philox key                                */
     uint64_t index_offset;   /* global element index of element 0         */
+    int32_t  hadamard;       /* 0, or the Walsh-Hadamard transform block H */
+    int32_t  reserved;
 } orc_params;
 
 /* IEEE-754 conversions written from the format definitions. */
@@ -62,7 +64,8 @@ int orc_unpack_dequant_reduce_requant(const uint8_t* const* codes_in,
                                       const orc_params* p_out,
                                       uint8_t* codes_out, uint16_t* scales_out);
 
-/* Encoder then single-rank decoder: deq_out = s*q per element. */
+/* Encoder then all-gather-side decode with mul = 1: deq_out = s*q per element
+ * (inverse-transformed when p->hadamard is set). */
 int orc_roundtrip(const void* x, int32_t dtype, int64_t n, float* err,
                   const orc_params* p, uint8_t* codes, uint16_t* scales, float* deq_out);
 
@@ -71,6 +74,10 @@ int orc_roundtrip(const void* x, int32_t dtype, int64_t n, float* err,
 int orc_unpack_dequant(const uint8_t* codes, const uint16_t* scales, int64_t n,
                        const orc_params* p, float mul, int32_t out_dtype, void* out);
 uint16_t orc_f32_to_bf16(float x);
+
+/* Unnormalised fast Walsh-Hadamard transform of every H-element block of
+ * x[0:n) in place (n a multiple of H). */
+int orc_fwht(float* x, int64_t n, int32_t H);
 
 /* Sizes. */
 int64_t orc_num_blocks(int64_t n, int32_t block);

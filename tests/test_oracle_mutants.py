@@ -18,7 +18,7 @@ MUTANTS = {
     "qmax_off_by_one": ("float qmax = (float)((1 << (bits - 1)) - 1);\n        x = amax / qmax;",
                         "float qmax = (float)((1 << (bits - 1)));\n        x = amax / qmax;"),
     "ef_sign": ("err_out[e] = val - d;", "err_out[e] = d - val;"),
-    "ef_add_dropped": ("v[i] = err ? (g + err[i]) : g;", "v[i] = g;"),
+    "ef_add_dropped": ("for (int64_t i = 0; i < n; ++i) v[i] = v[i] + err[i];", ";"),
     "ties_away_from_zero": ("if (frac > 0.5f) return f + 1.0f;", "if (frac >= 0.5f) return f + 1.0f;"),
     "msb_first_packing": ("(bit << (pos % 8))", "(bit << (7 - pos % 8))"),
     "sum_seeded_with_zero": ("acc = (w == 0) ? d : acc + d;", "acc = acc + d;"),
@@ -35,7 +35,11 @@ MUTANTS = {
                        "float acc = 0.0f; for (int64_t i = 0; i < n; ++i) acc += a[i]; return acc;"),
     "stage2_ef_dropped": ("r[i] = r[i] + err2[i];", "r[i] = r[i];"),
     "bf16_truncates": ("if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u))) kept += 1;", ";"),
-    "mul_inside_product": ("float y = d * mul;", "float y = s * ((float)q * mul);"),
+    "mul_inside_product": ("d[i] = s * (float)q;\n    }", "d[i] = s * ((float)q * mul);\n    }"),
+    "mul_applied_twice": ("float y = d[i] * mul;", "float y = d[i] * mul * mul;"),
+    "fwht_sign": ("x[j + h] = a - b;", "x[j + h] = b - a;"),
+    "inverse_without_1_over_H": ("for (int64_t i = 0; i < n; ++i) d[i] = d[i] * inv;", ";"),
+    "encoder_skips_rotation": ("if (p->hadamard) orc_fwht(v, n, p->hadamard);", ";"),
     "fma_in_feedback": ("float d = s * (float)q;          /* separate roundings, no FMA */\n                err_out[e] = val - d;",
                         "err_out[e] = fmaf(-s, (float)q, val);"),
 }

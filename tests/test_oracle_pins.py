@@ -544,3 +544,66 @@ def test_unpack_dequant_equals_single_rank_sum(orc, bits):
     torch = pytest.importorskip("torch")
     exp = torch.from_numpy(ref * np.float32(0.25)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(bf, exp)
+
+
+# ---- Hadamard smoothing (SDP4Bit README, "--hadamard-transform") -----------
+
+@pytest.mark.parametrize("H", [8, 16, 32, 64, 128, 256])
+def test_fwht_is_the_sylvester_hadamard_matrix(orc, H):
+    sla = pytest.importorskip("scipy.linalg")
+    rng = np.random.default_rng(H)
+    x = rng.integers(-1000, 1001, size=4 * H).astype(np.float32)   # sums stay exact in fp32
+    got = orc.fwht(x, H)
+    Hm = sla.hadamard(H).astype(np.float64)
+    ref = (x.reshape(4, H).astype(np.float64) @ Hm.T).reshape(-1)
+    np.testing.assert_array_equal(got.astype(np.float64), ref)
+    np.testing.assert_array_equal(orc.fwht(got, H) / np.float32(H), x)      # H H = H I
+
+
+def test_hadamard_hand_block(orc):
+    # x = e_0 in one block of 8: the transform is all ones, absmax 1, s =
+    # fp16(1/7) = 1170 * 2^-13 = 0.142822265625 (0x3092), every q = rint(7.0017)
+    # = 7 (code 15).  Decoding: d = 7s everywhere, the inverse transform puts
+    # 8 * 7s / 8 = 0.999755859375 at index 0 and exact zeros elsewhere.
+    x = np.zeros(8, np.float32)
+    x[0] = 1.0
+    p = orc.params(4, 8, hadamard=8)
+    codes, scales, deq = orc.roundtrip(x, p)
+    assert int(scales[0]) == 0x3092
+    assert codes.tobytes().hex() == "ffffffff"
+    assert deq.tolist() == [0.999755859375] + [0.0] * 7
+
+
+def test_decoder_does_not_transform(orc):
+    # The rank sum and the requantisation stay in the transformed domain:
+    # requantising one rank's own dequantised values with the same parameters
+    # reproduces its codes and scales exactly.
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal(4096).astype(np.float32)
+    p = orc.params(4, 128, hadamard=128)
+    c, s = orc.quantize_pack(x, p)
+    _, co, so = orc.unpack_dequant_reduce_requant([c], [s], 4096, p, False, None, p)
+    assert co.tobytes() == c.tobytes() and np.array_equal(so, s)
+    with pytest.raises(ValueError):   # stages must share the transform
+        orc.unpack_dequant_reduce_requant([c], [s], 4096, p, False, None, orc.params(4, 128))
+
+
+def test_hadamard_reduces_error_on_outlier_blocks(orc):
+    # The page's stated purpose: the rotation spreads an outlier over its block,
+    # so the 4-bit roundtrip error of outlier-heavy gradients drops.
+    rng = np.random.default_rng(3)
+    n = 1 << 16
+    x = (rng.standard_normal(n) * 1e-4).astype(np.float32)
+    x[rng.integers(0, n, n // 128)] *= 100.0
+    plain = orc.roundtrip(x, orc.params(4, 128))[2]
+    rot = orc.roundtrip(x, orc.params(4, 128, hadamard=128))[2]
+    e_plain = np.linalg.norm(plain.astype(np.float64) - x)
+    e_rot = np.linalg.norm(rot.astype(np.float64) - x)
+    assert e_rot < 0.7 * e_plain, (e_rot, e_plain)
+
+
+def test_hadamard_rejects_bad_sizes(orc):
+    with pytest.raises(ValueError):
+        orc.quantize_pack(np.zeros(100, np.float32), orc.params(4, 128, hadamard=128))   # n % H
+    with pytest.raises(ValueError):
+        orc.quantize_pack(np.zeros(128, np.float32), orc.params(4, 64, hadamard=128))    # H > B
