@@ -127,45 +127,52 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 class AllReduceW8:
-    """Device buffers and the launch sequence of one simulated all-reduce."""
+    """Device buffers and the launch sequence of one simulated all-reduce.
+    p1 / p2 default to the headline parameters (4-bit, block 128, RTN)."""
 
-    def __init__(self, torch, bc, synth, n, W, device):
+    def __init__(self, torch, bc, synth, n, W, device, p1=None, p2=None):
         self.torch, self.bc, self.n, self.W = torch, bc, n, W
-        self.p1 = [bc.QParams(BITS, BLOCK, bc.RTN, seed=1000 + w) for w in range(W)]
-        self.p2 = bc.QParams(BITS, BLOCK, bc.RTN, philox_stream=1)
+        base1 = p1 or bc.QParams(BITS, BLOCK, bc.RTN)
+        self.p1 = [bc.QParams(base1.bits, base1.block, base1.rounding, seed=1000 + w,
+                              hadamard=base1.hadamard) for w in range(W)]
+        self.p2 = p2 or bc.QParams(BITS, BLOCK, bc.RTN, philox_stream=1)
         self.x = [synth.gradients("normal", n, 1000 + w, dtype=torch.bfloat16, device=device, sigma=1e-3)
                   for w in range(W)]
         self.err = [torch.zeros(n, dtype=torch.float32, device=device) for _ in range(W)]
         self.codes, self.scales = zip(*[bc.alloc_codes(n, self.p1[0], device) for _ in range(W)])
         self.err2 = torch.zeros(n, dtype=torch.float32, device=device)
         self.codes_out, self.scales_out = bc.alloc_codes(n, self.p2, device)
-        nb = bc.num_blocks(n, BLOCK)
-        cb = (nb + W - 1) // W
+        B1, B2 = self.p1[0].block, self.p2.block
+        U = max(B1, B2)                          # chunks are whole blocks of both stages
+        units = (n + U - 1) // U
+        cu = (units + W - 1) // W
         self.chunks = []
         for c in range(W):
-            b0, b1 = c * cb, min((c + 1) * cb, nb)
-            if b0 >= b1:
+            u0, u1 = c * cu, min((c + 1) * cu, units)
+            if u0 >= u1:
                 break
-            lo, hi = b0 * BLOCK, min(b1 * BLOCK, n)
-            self.chunks.append((lo, hi, b0, b1))
+            self.chunks.append((u0 * U, min(u1 * U, n)))
 
     def encode(self, stream=None):
         for w in range(self.W):
-            self.bc.quantize_pack(self.x[w], self.p1[w], self.err[w], self.codes[w], self.scales[w],
-                                  stream=stream)
+            self.encode_rank(w, stream)
 
     def encode_rank(self, w, stream=None):
         self.bc.quantize_pack(self.x[w], self.p1[w], self.err[w], self.codes[w], self.scales[w],
                               stream=stream)
 
     def decode(self, stream=None):
-        for lo, hi, b0, b1 in self.chunks:
-            cin = [c[lo * BITS // 8: b1 * BLOCK * BITS // 8] for c in self.codes]
-            sin = [s[b0:b1] for s in self.scales]
+        b1, B1 = self.p1[0].bits, self.p1[0].block
+        b2, B2 = self.p2.bits, self.p2.block
+        for lo, hi in self.chunks:
+            hi1 = (hi + B1 - 1) // B1 * B1
+            hi2 = (hi + B2 - 1) // B2 * B2
+            cin = [c[lo * b1 // 8: hi1 * b1 // 8] for c in self.codes]
+            sin = [s[lo // B1: hi1 // B1] for s in self.scales]
             self.bc.unpack_dequant_reduce_requant(
                 cin, sin, hi - lo, self.p1[0], sum_out=None, err2=self.err2[lo:hi],
-                p_out=self.p2.shifted(lo), codes_out=self.codes_out[lo * BITS // 8: b1 * BLOCK * BITS // 8],
-                scales_out=self.scales_out[b0:b1], stream=stream)
+                p_out=self.p2.shifted(lo), codes_out=self.codes_out[lo * b2 // 8: hi2 * b2 // 8],
+                scales_out=self.scales_out[lo // B2: hi2 // B2], stream=stream)
 
 
 def run_ours(args, rank, world, local_rank):
@@ -519,6 +526,27 @@ def run_workload(args):
         t = _timed(torch, step, K)
         algo = wl.n * (wl.bits / 8 + 2 / wl.block + 2)
         extra = {"l2": "inputs larger than L2 (3.3 GB per step)", "output": "bf16", "mul": "1/8"}
+    elif args.workload == "tlq_hs_w8_gpt1p3b":
+        # two-level quantisation with Hadamard smoothing: stage 1 8-bit groups of
+        # 512, stage 2 4-bit groups of 128, both rotated by H = 128
+        p1 = bc.QParams(8, 512, bc.RTN, hadamard=128)
+        p2 = bc.QParams(4, 128, bc.RTN, philox_stream=1, hadamard=128)
+        ar = AllReduceW8(torch, bc, synth, wl.n, wl.ranks, torch.device("cuda"), p1, p2)
+        for _ in range(warm):
+            ar.encode()
+            ar.decode()
+        te = _timed(torch, ar.encode, K)
+        td = _timed(torch, ar.decode, K)
+        t = te + td
+        enc_b = wl.n * (2 + 8 + 1 + 2 / 512)
+        dec_b = wl.n / len(ar.chunks) * (8 * (1 + 2 / 512) + 8 + 0.5 + 2 / 128)
+        enc_gbs = enc_b / (te / wl.ranks) / 1e6
+        dec_gbs = dec_b / (td / len(ar.chunks)) / 1e6
+        algo = wl.n * wl.ranks * (2 + 8 + 1 + 2 / 512) + wl.n * (8 * (1 + 2 / 512) + 8 + 0.5 + 2 / 128)
+        extra = {"l2": "inputs larger than L2", "stage1": "8-bit B512 H128 EF", "stage2": "4-bit B128 H128 EF2",
+                 "encode_gbs": round(enc_gbs, 1), "encode_frac": round(enc_gbs / peak, 4),
+                 "decode_gbs": round(dec_gbs, 1), "decode_frac": round(dec_gbs / peak, 4)}
+        wl_elems = wl.n * wl.ranks
     elif args.workload == "gpt6p7b_2bit_buckets":
         sched = bc.Scheduler(2, wl.bucket_bytes)
         x = synth.gradients(wl.kind, wl.n, wl.seed, dtype=dt, **wl.params)
@@ -534,7 +562,8 @@ def run_workload(args):
     else:
         raise SystemExit(f"workload {args.workload}: use the default run")
     gbs = algo / t / 1e6
-    out = {"metric": METRIC, "value": round(wl.n * 4 / t / 1e6, 2), "unit": UNIT, "n_gpus": 1, "steps": K,
+    elems = locals().get("wl_elems", wl.n)
+    out = {"metric": METRIC, "value": round(elems * 4 / t / 1e6, 2), "unit": UNIT, "n_gpus": 1, "steps": K,
            "warmup": warm, "ms_per_step": round(t, 4), "higher_is_better": True, "dtype": "f32",
            "data": "synthetic", "config": {"workload": wl.name, "n": wl.n, "input_dtype": wl.dtype,
                                            "bits": wl.bits, "block": wl.block, **extra},

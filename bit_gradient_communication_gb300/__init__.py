@@ -44,28 +44,31 @@ class BitscomError(RuntimeError):
 class _QParams(ctypes.Structure):
     _fields_ = [("bits", ctypes.c_int32), ("block", ctypes.c_int32),
                 ("rounding", ctypes.c_int32), ("philox_stream", ctypes.c_uint32),
-                ("seed", ctypes.c_uint64), ("index_offset", ctypes.c_uint64)]
+                ("seed", ctypes.c_uint64), ("index_offset", ctypes.c_uint64),
+                ("hadamard", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 @dataclass
 class QParams:
     """One quantisation stage: bits in {1,2,4,8,12,16}, block a power of two in
-    [8, 4096], rounding RTN or SR, Philox seed / stream word, and the global
-    element index of the call's first element."""
+    [8, 4096], rounding RTN or SR, Philox seed / stream word, the global
+    element index of the call's first element, and the Walsh-Hadamard
+    transform block (0 = none)."""
     bits: int
     block: int
     rounding: int = RTN
     seed: int = 0
     index_offset: int = 0
     philox_stream: int = 0
+    hadamard: int = 0
 
     def c(self) -> _QParams:
         return _QParams(self.bits, self.block, self.rounding, self.philox_stream,
-                        self.seed, self.index_offset)
+                        self.seed, self.index_offset, self.hadamard, 0)
 
     def shifted(self, offset: int) -> "QParams":
         return QParams(self.bits, self.block, self.rounding, self.seed,
-                       self.index_offset + offset, self.philox_stream)
+                       self.index_offset + offset, self.philox_stream, self.hadamard)
 
 
 _lock = threading.Lock()

@@ -31,10 +31,26 @@ int log2_block(int B)
     return l;
 }
 
+bool valid_hadamard(int H, int B)
+{
+    return H == 0 || (H >= 8 && H <= 256 && (H & (H - 1)) == 0 && B % H == 0);
+}
+
 bool valid_params(const bitscom_qparams* p)
 {
     return p && valid_bits(p->bits) && log2_block(p->block) >= 0 &&
-           (p->rounding == BITSCOM_RTN || p->rounding == BITSCOM_SR);
+           (p->rounding == BITSCOM_RTN || p->rounding == BITSCOM_SR) &&
+           valid_hadamard(p->hadamard, p->block) && p->reserved == 0;
+}
+
+// The Walsh-Hadamard rotation needs whole transform blocks and has kernels
+// for 2-, 4- and 8-bit codes.
+bitscom_status check_hadamard(const bitscom_qparams* p, int64_t n)
+{
+    if (!p->hadamard) return BITSCOM_OK;
+    if (n % p->hadamard != 0) return BITSCOM_EINVAL;
+    if (p->bits != 2 && p->bits != 4 && p->bits != 8) return BITSCOM_EUNSUPPORTED;
+    return BITSCOM_OK;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -62,6 +78,8 @@ bitscom_status check_encode(const void* x, bitscom_dtype dt, int64_t n, const fl
     if (!valid_params(p) || n < 0 || (dt != BITSCOM_F32 && dt != BITSCOM_BF16)) return BITSCOM_EINVAL;
     if (n == 0) return BITSCOM_OK;
     if (!x || !codes || !scales) return BITSCOM_EINVAL;
+    const bitscom_status h = check_hadamard(p, n);
+    if (h != BITSCOM_OK) return h;
     if (!aligned(x, dt == BITSCOM_F32 ? 32 : 16) || (err && !aligned(err, 32)) ||
         !aligned(codes, code_align(p->bits)) || !aligned(scales, 2))
         return BITSCOM_EALIGN;
@@ -75,6 +93,7 @@ bitscom_status check_decode(const void* const* codes_in, const uint16_t* const* 
 {
     if (!valid_params(p_in) || n < 0 || W < 1 || W > kMaxRanks) return BITSCOM_EINVAL;
     if (p_out && !valid_params(p_out)) return BITSCOM_EINVAL;
+    if (p_out && p_out->hadamard != p_in->hadamard) return BITSCOM_EINVAL;   // one rotated domain
     if (err2 && !p_out) return BITSCOM_EINVAL;
     if (!sum_out && !p_out) return BITSCOM_EINVAL;
     if (n == 0) return BITSCOM_OK;
@@ -143,6 +162,7 @@ bitscom_status bitscom_quantize_pack(const void* x, bitscom_dtype dt, int64_t n,
     a.philox_stream = p->philox_stream;
     a.seed = p->seed;
     a.index_offset = p->index_offset;
+    a.hadamard = p->hadamard;
     return cuda_status(bitscom::launch_encode(a, dt == BITSCOM_F32 ? 0 : 1, p->bits,
                                               p->rounding == BITSCOM_SR,
                                               static_cast<cudaStream_t>(cuda_stream)));
@@ -188,6 +208,8 @@ bitscom_status bitscom_unpack_dequant(const void* codes, const uint16_t* scales,
     if (!valid_params(p) || n < 0 || (out_dt != BITSCOM_F32 && out_dt != BITSCOM_BF16)) return BITSCOM_EINVAL;
     if (n == 0) return BITSCOM_OK;
     if (!codes || !scales || !out) return BITSCOM_EINVAL;
+    const bitscom_status h = check_hadamard(p, n);
+    if (h != BITSCOM_OK) return h;
     if (!aligned(codes, code_align(p->bits)) || !aligned(scales, 2) ||
         !aligned(out, out_dt == BITSCOM_F32 ? 32 : 16))
         return BITSCOM_EALIGN;
@@ -198,6 +220,7 @@ bitscom_status bitscom_unpack_dequant(const void* codes, const uint16_t* scales,
     a.log2B = log2_block(p->block);
     a.mul = mul;
     a.out = out;
+    a.hadamard = p->hadamard;
     return cuda_status(bitscom::launch_dequant(a, p->bits, out_dt == BITSCOM_F32 ? 0 : 1,
                                                static_cast<cudaStream_t>(cuda_stream)));
 }
@@ -210,10 +233,7 @@ bitscom_status bitscom_roundtrip(const void* x, bitscom_dtype dt, int64_t n, flo
     if (deq_out && !aligned(deq_out, 32)) return BITSCOM_EALIGN;
     bitscom_status s = bitscom_quantize_pack(x, dt, n, err, p, codes_tmp, scales_tmp, cuda_stream);
     if (s != BITSCOM_OK || n == 0) return s;
-    const void* c[1] = {codes_tmp};
-    const uint16_t* sc[1] = {scales_tmp};
-    return bitscom_unpack_dequant_reduce_requant(c, sc, 1, n, p, deq_out, nullptr, nullptr, nullptr,
-                                                 nullptr, cuda_stream);
+    return bitscom_unpack_dequant(codes_tmp, scales_tmp, n, p, 1.0f, BITSCOM_F32, deq_out, cuda_stream);
 }
 
 }  // extern "C"

@@ -12,7 +12,9 @@
 
 namespace bitscom {
 
-template <int BITS, int OUT>   // OUT: 0 = fp32, 1 = bf16
+// OUT: 0 = fp32, 1 = bf16.  HAD: inverse Walsh-Hadamard rotation of every
+// a.hadamard-element block (the same transform, then the exact factor 1/H).
+template <int BITS, int OUT, bool HAD>
 __global__ void __launch_bounds__(kThreads, 2) dequant_kernel(const DqArgs a)
 {
     const int64_t n = a.n;
@@ -47,6 +49,12 @@ __global__ void __launch_bounds__(kThreads, 2) dequant_kernel(const DqArgs a)
             for (int j = 0; j < 8; ++j) d[j] = __fmul_rn(s, l[j]);
         }
         if (row + gridDim.x < rows) load(row + gridDim.x);   // prefetch the next row
+        if constexpr (HAD) {
+            fwht8(d, a.hadamard);
+            const float inv = 1.0f / (float)a.hadamard;          // a power of two: exact
+#pragma unroll
+            for (int j = 0; j < 8; ++j) d[j] = __fmul_rn(d[j], inv);
+        }
         float y[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) y[j] = __fmul_rn(d[j], a.mul);
@@ -77,14 +85,25 @@ __global__ void __launch_bounds__(kThreads, 2) dequant_kernel(const DqArgs a)
     }
 }
 
-template <int BITS, int OUT>
-static cudaError_t run_dequant(const DqArgs& a, cudaStream_t st)
+template <int BITS, int OUT, bool HAD>
+static cudaError_t run_dequant_h(const DqArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};
     const int64_t rows = (a.n + kRow - 1) / kRow;
-    const int grid = grid_size(dequant_kernel<BITS, OUT>, cap, rows);
-    dequant_kernel<BITS, OUT><<<grid, kThreads, 0, st>>>(a);
+    const int grid = grid_size(dequant_kernel<BITS, OUT, HAD>, cap, rows);
+    dequant_kernel<BITS, OUT, HAD><<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
+}
+
+template <int BITS, int OUT>
+static cudaError_t run_dequant(const DqArgs& a, cudaStream_t st)
+{
+    if (a.hadamard == 0) return run_dequant_h<BITS, OUT, false>(a, st);
+    if constexpr (BITS == 2 || BITS == 4 || BITS == 8) {
+        return run_dequant_h<BITS, OUT, true>(a, st);
+    } else {
+        return cudaErrorNotSupported;
+    }
 }
 
 template <int OUT>

@@ -54,9 +54,11 @@ __device__ __forceinline__ void load_row(const EncArgs& a, int64_t row, RowIn<IN
     }
 }
 
-// IN: 0 = fp32, 1 = bf16.  The row loop is software-pipelined: the loads of
-// row r + gridDim.x are issued before row r is computed.
-template <int IN, int BITS, bool EF, bool SR>
+// IN: 0 = fp32, 1 = bf16.  HAD: rotate every a.hadamard-element block of g by
+// the Walsh-Hadamard transform before the error is added.  The row loop is
+// software-pipelined: the loads of row r + gridDim.x are issued before row r
+// is computed.
+template <int IN, int BITS, bool EF, bool SR, bool HAD>
 __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
 {
     __shared__ float red[2][kWarps];
@@ -82,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
         } else {
             bf16x8_to_f32(cur.gb, v);
         }
+        if constexpr (HAD) fwht8(v, a.hadamard);
         if constexpr (EF) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) v[j] = __fadd_rn(v[j], cur.e[j]);
@@ -137,14 +140,26 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
     }
 }
 
-template <int IN, int BITS, bool EF, bool SR>
-static cudaError_t run_encode(const EncArgs& a, cudaStream_t st)
+template <int IN, int BITS, bool EF, bool SR, bool HAD>
+static cudaError_t run_encode_h(const EncArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};   // SMs x resident CTAs of this instantiation
     const int64_t rows = (a.n + kRow - 1) / kRow;
-    const int grid = grid_size(encode_kernel<IN, BITS, EF, SR>, cap, rows);
-    encode_kernel<IN, BITS, EF, SR><<<grid, kThreads, 0, st>>>(a);
+    const int grid = grid_size(encode_kernel<IN, BITS, EF, SR, HAD>, cap, rows);
+    encode_kernel<IN, BITS, EF, SR, HAD><<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
+}
+
+// The Hadamard rotation has instantiations for 2-, 4- and 8-bit codes.
+template <int IN, int BITS, bool EF, bool SR>
+static cudaError_t run_encode(const EncArgs& a, cudaStream_t st)
+{
+    if (a.hadamard == 0) return run_encode_h<IN, BITS, EF, SR, false>(a, st);
+    if constexpr (BITS == 2 || BITS == 4 || BITS == 8) {
+        return run_encode_h<IN, BITS, EF, SR, true>(a, st);
+    } else {
+        return cudaErrorNotSupported;
+    }
 }
 
 template <int IN, int BITS>

@@ -20,6 +20,7 @@ struct EncArgs {
     uint32_t philox_stream;
     uint64_t seed;
     uint64_t index_offset;
+    int hadamard;           // 0 or the transform block H
 };
 
 constexpr int kMaxRanks = 64;
@@ -48,6 +49,7 @@ struct DqArgs {
     int log2B;
     float mul;
     void* out;              // fp32 or bf16 [n]
+    int hadamard;           // 0 or the transform block H (inverse applied)
 };
 
 // Return cudaErrorNotSupported for a combination without a kernel.

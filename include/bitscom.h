@@ -34,6 +34,13 @@
  *   Error feedback: v = fl(g + e); e' = fl(v - fl(s*q)) (no fused multiply-add).
  *   Reduce: r = d_0, r = fl(r + d_w) for w = 1..W-1 (rank order, fp32), with
  *           d_w = fl(s_w * q_w); stage 2 adds e2: v2 = fl(r + e2).
+ *   Hadamard smoothing (SDP4Bit README, "--hadamard-transform"; optional):
+ *           the encoder rotates every H-element block of g by the unnormalised
+ *           Sylvester Walsh-Hadamard transform (stage h = 1, 2, 4, ...: x_i,
+ *           x_{i+h} -> x_i + x_{i+h}, x_i - x_{i+h} in fp32) before adding e;
+ *           error feedback, the rank sum and the requantisation stay in the
+ *           rotated domain; bitscom_unpack_dequant applies the inverse (the
+ *           same transform, then 1/H).
  *
  * Memory: the caller allocates and owns every buffer (device memory unless
  * stated) and the CUDA stream.  Calls are asynchronous on the given stream
@@ -83,6 +90,12 @@ typedef struct {
     uint32_t philox_stream;  /* Philox counter word 2 (0 = stage 1, 1 = stage 2)    */
     uint64_t seed;           /* Philox key                                          */
     uint64_t index_offset;   /* global element index of element 0 of this call      */
+    int32_t  hadamard;       /* 0, or H: rotate every H-element block by the        */
+                             /* Walsh-Hadamard transform (H a power of two in        */
+                             /* [8, 256] dividing block; bits 2, 4 or 8; n a         */
+                             /* multiple of H).  Every stage of one all-reduce uses  */
+                             /* the same H.                                          */
+    int32_t  reserved;       /* must be 0                                           */
 } bitscom_qparams;
 
 /* Number of blocks ceil(n / block). */

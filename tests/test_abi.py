@@ -171,3 +171,27 @@ def test_binding_refuses_cpu_tensors(bc):
     torch = pytest.importorskip("torch")
     with pytest.raises(ValueError, match="CUDA"):
         bc.quantize_pack(torch.zeros(16), bc.QParams(4, 8))
+
+
+def test_hadamard_argument_checks(bc):
+    L = bc.lib()
+    def call(bits=4, block=128, H=128, n=1024, reserved=0):
+        q = bc.QParams(bits, block, hadamard=H).c()
+        q.reserved = reserved
+        return L.bitscom_quantize_pack(_fake(0x10000), 0, n, None, ctypes.byref(q), _fake(0x20000),
+                                       _fake(0x30000), None)
+    assert call(H=4) == 1            # below 8
+    assert call(H=96) == 1           # not a power of two
+    assert call(H=512, block=512) == 1   # above 256
+    assert call(H=128, block=64) == 1    # does not divide the block
+    assert call(n=1000) == 1         # n not a multiple of H
+    assert call(reserved=1) == 1
+    assert call(bits=12) == 3        # no rotated kernel for 12-bit codes
+    # decoder: both stages must share the rotation
+    codes = (ctypes.c_void_p * 1)(0x10000)
+    scales = (ctypes.c_void_p * 1)(0x40000)
+    st = L.bitscom_unpack_dequant_reduce_requant(
+        ctypes.cast(codes, ctypes.c_void_p), ctypes.cast(scales, ctypes.c_void_p), 1, 1024,
+        ctypes.byref(bc.QParams(4, 128, hadamard=128).c()), None, None,
+        ctypes.byref(bc.QParams(4, 128).c()), _fake(0x20000), _fake(0x30000), None)
+    assert st == 1

@@ -88,7 +88,7 @@ def test_allreduce_w8_gpt1p3b_windows():
     ar.decode()
     torch.cuda.synchronize()
     B = bench.BLOCK
-    bounds = [b0 for (_, _, b0, _) in ar.chunks]
+    bounds = [lo // B for (lo, _) in ar.chunks]
     for lo, hi, b0 in _windows(n, B, 48, 64, 3, bounds):
         m = hi - lo
         enc = []

@@ -257,3 +257,47 @@ def test_allgather_decode_matches_oracle(bits, block, out):
         ref = O.unpack_dequant(codes, scales, n, O.params(bits, block), mul, O.F32 if out == "f32" else O.BF16)
         got = og.host(np.uint32 if out == "f32" else np.uint16)
         assert np.array_equal(got, ref.view(np.uint32 if out == "f32" else np.uint16)), f"n={n} mul={mul}"
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("H,block", [(8, 8), (32, 128), (128, 128), (128, 512), (256, 4096)])
+@pytest.mark.parametrize("mode", ["rtn", "sr_ef"])
+def test_hadamard_encoder_and_decode_match_oracle(dt, bits, H, block, mode):
+    # Walsh-Hadamard smoothing: rotated encoder (error feedback in the rotated
+    # domain) and the all-gather-side decode with the inverse rotation.
+    torch, bc = need_gpu()
+    sr, ef = mode.startswith("sr"), mode.endswith("ef")
+    for k, n in enumerate([block, 3 * 4096 + 2 * block, 6 * 4096]):
+        x, e = _inputs(n, dt, seed=bits * 100 + H + k)
+        xh = x if dt == "f32" else bf16_bits_of(torch, x)
+        p = bc.QParams(bits, block, bc.SR if sr else bc.RTN, seed=5 + k, index_offset=4 * k, hadamard=H)
+        po = O.params(bits, block, O.SR if sr else O.RTN, seed=5 + k, index_offset=4 * k, hadamard=H)
+        codes, scales, err = _run_encode(torch, bc, xh, dt, n, p, e.copy() if ef else None)
+        e_ref = e.copy() if ef else None
+        c_ref, s_ref = O.quantize_pack(xh, po, e_ref)
+        assert codes.tobytes() == c_ref.tobytes(), f"codes n={n}"
+        assert np.array_equal(scales, s_ref), f"scales n={n}"
+        if ef:
+            assert np.array_equal(err.view(np.uint32), e_ref.view(np.uint32)), f"e' n={n}"
+        for out in ("f32", "bf16"):
+            dst = torch.empty(n, dtype=torch.float32 if out == "f32" else torch.bfloat16, device="cuda")
+            bc.unpack_dequant(torch.from_numpy(codes).cuda(), torch.from_numpy(scales.view(np.int16)).cuda(),
+                              n, p, 0.5, out=dst)
+            ref = O.unpack_dequant(codes, scales, n, po, 0.5, O.F32 if out == "f32" else O.BF16)
+            got = dst.view(torch.int32 if out == "f32" else torch.int16).cpu().numpy()
+            assert np.array_equal(got.view(np.uint32 if out == "f32" else np.uint16),
+                                  ref.view(np.uint32 if out == "f32" else np.uint16)), f"{out} n={n}"
+
+
+def test_hadamard_roundtrip_matches_oracle():
+    torch, bc = need_gpu()
+    n = 8 * 4096
+    x, e = _inputs(n, "f32", 3)
+    p = bc.QParams(4, 128, hadamard=128)
+    eg = torch.from_numpy(e.copy()).cuda()
+    deq = bc.roundtrip(torch.from_numpy(x).cuda(), p, err=eg)
+    e_ref = e.copy()
+    _, _, d_ref = O.roundtrip(x, O.params(4, 128, hadamard=128), e_ref)
+    assert np.array_equal(deq.cpu().numpy().view(np.uint32), d_ref.view(np.uint32))
+    assert np.array_equal(eg.cpu().numpy().view(np.uint32), e_ref.view(np.uint32))

@@ -174,3 +174,33 @@ def test_allreduce_then_allgather_decode_matches_oracle():
     ref = O.unpack_dequant(c_ref, s_ref, n, O.params(4, 128), float(np.float32(1.0 / W)), O.BF16)
     assert np.array_equal(_host_bits(mean), ref)
     sched.close()
+
+
+def test_two_level_hadamard_allreduce_matches_oracle():
+    # SDP4Bit-style two-level quantisation with Hadamard smoothing: stage 1
+    # 8-bit groups of 512, stage 2 4-bit groups of 128, both rotated by H = 128;
+    # then the all-gather-side decode back to the bf16 mean gradient.
+    _, bc = need_gpu()
+    W, n = 8, 16 * 4096
+    sched = bc.Scheduler(n_streams=2, bucket_bytes=0)
+    xs = [_x(n, 70 + w, "bf16") for w in range(W)]
+    errs = [torch.zeros(n, device="cuda") for _ in range(W)]
+    p1 = [bc.QParams(8, 512, bc.RTN, hadamard=128) for _ in range(W)]
+    p2 = bc.QParams(4, 128, bc.SR, seed=11, philox_stream=1, hadamard=128)
+    codes, scales = zip(*[bc.alloc_codes(n, p1[0]) for _ in range(W)])
+    err2 = torch.zeros(n, device="cuda")
+    co, so = bc.alloc_codes(n, p2)
+    sched.allreduce(xs, p1, codes, scales, errs, p2, err2, co, so)
+    mean = bc.unpack_dequant(co, so, n, p2, mul=1.0 / W, out_dtype=torch.bfloat16)
+    sched.wait()
+    torch.cuda.synchronize()
+    h_err = [np.zeros(n, np.float32) for _ in range(W)]
+    h_e2 = np.zeros(n, np.float32)
+    o1 = [O.params(8, 512, hadamard=128) for _ in range(W)]
+    o2 = O.params(4, 128, O.SR, seed=11, philox_stream=1, hadamard=128)
+    _, _, c_ref, s_ref = _oracle_allreduce([_host_bits(x) for x in xs], n, W, o1, o2, h_err, h_e2)
+    assert co.cpu().numpy().tobytes() == c_ref.tobytes()
+    assert np.array_equal(err2.cpu().numpy().view(np.uint32), h_e2.view(np.uint32))
+    ref = O.unpack_dequant(c_ref, s_ref, n, o2, float(np.float32(1.0 / W)), O.BF16)
+    assert np.array_equal(_host_bits(mean), ref)
+    sched.close()
