@@ -14,6 +14,7 @@ Parity status of each function (details in the tests):
                                          telescoping error-feedback bound)
   unpack_dequant, f32_to_bf16            pinned (W=1 decoder sums, torch bf16 cast)
   fwht (Hadamard smoothing)              pinned (scipy Sylvester matrix, involution)
+  qwd_encode, qwd_apply                  pinned (hand block, bound, telescoping)
   tail blocks (n mod B != 0), 1-bit SR   parity unpinned (readings only)
 """
 from __future__ import annotations
@@ -95,6 +96,10 @@ def lib():
             L.orc_unpack_dequant.argtypes = [vp, vp, i64, P, ctypes.c_float, i32, vp]
             L.orc_f32_to_bf16.restype = ctypes.c_uint16
             L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+            L.orc_qwd_encode.restype = ctypes.c_int
+            L.orc_qwd_encode.argtypes = [vp, i32, i64, vp, P, vp, vp]
+            L.orc_qwd_apply.restype = ctypes.c_int
+            L.orc_qwd_apply.argtypes = [vp, vp, i64, P, vp, vp, i32]
             L.orc_fwht.restype = ctypes.c_int
             L.orc_fwht.argtypes = [vp, i64, i32]
             L.orc_num_blocks.restype = i64
@@ -210,6 +215,31 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     L = lib()
     return np.array([L.orc_f32_to_bf16(float(v)) for v in x], dtype=np.uint16)
+
+
+def qwd_encode(w: np.ndarray, ref: np.ndarray, p: Params):
+    """Weight-difference encoder: codes of w - ref; ref advances in place."""
+    w = np.ascontiguousarray(w)
+    n = w.size
+    assert ref.dtype == np.float32 and ref.flags.c_contiguous and ref.size == n
+    codes = np.zeros(packed_bytes(n, p.bits, p.block), dtype=np.uint8)
+    scales = np.zeros(num_blocks(n, p.block), dtype=np.uint16)
+    if lib().orc_qwd_encode(_ptr(w), _dtype_code(w), n, _ptr(ref), ctypes.byref(p), _ptr(codes), _ptr(scales)):
+        raise ValueError("oracle rejected the arguments")
+    return codes, scales
+
+
+def qwd_apply(codes, scales, n: int, p: Params, ref: np.ndarray, w_dtype=None):
+    """Receiver update ref += s*q in place; returns the weights (fp32 or bf16 bits) or None."""
+    out = None
+    if w_dtype is not None:
+        out = np.zeros(n, dtype=np.float32 if w_dtype == F32 else np.uint16)
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    if lib().orc_qwd_apply(_ptr(codes), _ptr(scales), n, ctypes.byref(p), _ptr(ref), _ptr(out),
+                           0 if w_dtype in (None, F32) else 1):
+        raise ValueError("oracle rejected the arguments")
+    return out
 
 
 def fwht(x: np.ndarray, H: int) -> np.ndarray:

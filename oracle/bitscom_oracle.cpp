@@ -443,6 +443,47 @@ int orc_unpack_dequant(const uint8_t* codes, const uint16_t* scales, int64_t n,
     return 0;
 }
 
+/* SDP4Bit README, "Weight Quantization Arguments" (--quantized-weights,
+ * --weight-quantization-bits, --wq-group-size) and its overview ("quantization
+ * on weight differences").  Reading: the difference is taken against the
+ * reference copy every rank already holds (the last broadcast weights), the
+ * reference advances by the dequantised difference on every rank -- the
+ * sender included, so all copies stay bit-identical -- and the quantisation
+ * residual stays in w - ref for the next step.  No Hadamard rotation here. */
+int orc_qwd_encode(const void* w, int32_t dtype, int64_t n, float* ref, const orc_params* p,
+                   uint8_t* codes, uint16_t* scales)
+{
+    if (!valid_params(p) || p->hadamard || n < 0 || (dtype != 0 && dtype != 1)) return 1;
+    if (n == 0) return 0;
+    if (!w || !ref || !codes || !scales) return 1;
+    float* d = new float[n];
+    for (int64_t i = 0; i < n; ++i) {
+        float wi = (dtype == 0) ? ((const float*)w)[i] : orc_bf16_to_f32(((const uint16_t*)w)[i]);
+        d[i] = wi - ref[i];
+    }
+    quantize_stage(d, n, p, NULL, codes, scales);
+    delete[] d;
+    return orc_qwd_apply(codes, scales, n, p, ref, NULL, 0);
+}
+
+int orc_qwd_apply(const uint8_t* codes, const uint16_t* scales, int64_t n, const orc_params* p,
+                  float* ref, void* w_out, int32_t w_dtype)
+{
+    if (!valid_params(p) || p->hadamard || n < 0 || (w_dtype != 0 && w_dtype != 1)) return 1;
+    if (n == 0) return 0;
+    if (!codes || !scales || !ref) return 1;
+    for (int64_t i = 0; i < n; ++i) {
+        float s = orc_f16_to_f32(scales[i / p->block]);
+        int32_t q = code_to_q(get_code(codes, i, p->bits), p->bits);
+        ref[i] = ref[i] + s * (float)q;
+        if (w_out) {
+            if (w_dtype == 0) ((float*)w_out)[i] = ref[i];
+            else ((uint16_t*)w_out)[i] = orc_f32_to_bf16(ref[i]);
+        }
+    }
+    return 0;
+}
+
 int orc_roundtrip(const void* x, int32_t dtype, int64_t n, float* err,
                   const orc_params* p, uint8_t* codes, uint16_t* scales, float* deq_out)
 {

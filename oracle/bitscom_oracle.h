@@ -75,6 +75,15 @@ int orc_unpack_dequant(const uint8_t* codes, const uint16_t* scales, int64_t n,
                        const orc_params* p, float mul, int32_t out_dtype, void* out);
 uint16_t orc_f32_to_bf16(float x);
 
+/* Weight-difference quantisation for the sharded weight all-gather.
+ * Sender: d = fl(w - ref) quantised (codes, scales); ref = fl(ref + fl(s*q)).
+ * Receiver (every rank, on the gathered codes): ref = fl(ref + fl(s*q)), and
+ * optionally w_out = ref as fp32 (w_dtype 0) or bf16 bits (1). */
+int orc_qwd_encode(const void* w, int32_t dtype, int64_t n, float* ref, const orc_params* p,
+                   uint8_t* codes, uint16_t* scales);
+int orc_qwd_apply(const uint8_t* codes, const uint16_t* scales, int64_t n, const orc_params* p,
+                  float* ref, void* w_out, int32_t w_dtype);
+
 /* Unnormalised fast Walsh-Hadamard transform of every H-element block of
  * x[0:n) in place (n a multiple of H). */
 int orc_fwht(float* x, int64_t n, int32_t H);

@@ -40,6 +40,8 @@ MUTANTS = {
     "fwht_sign": ("x[j + h] = a - b;", "x[j + h] = b - a;"),
     "inverse_without_1_over_H": ("for (int64_t i = 0; i < n; ++i) d[i] = d[i] * inv;", ";"),
     "encoder_skips_rotation": ("if (p->hadamard) orc_fwht(v, n, p->hadamard);", ";"),
+    "qwd_reference_not_advanced": ("return orc_qwd_apply(codes, scales, n, p, ref, NULL, 0);", "return 0;"),
+    "qwd_difference_sign": ("d[i] = wi - ref[i];", "d[i] = ref[i] - wi;"),
     "fma_in_feedback": ("float d = s * (float)q;          /* separate roundings, no FMA */\n                err_out[e] = val - d;",
                         "err_out[e] = fmaf(-s, (float)q, val);"),
 }

@@ -607,3 +607,39 @@ def test_hadamard_rejects_bad_sizes(orc):
         orc.quantize_pack(np.zeros(100, np.float32), orc.params(4, 128, hadamard=128))   # n % H
     with pytest.raises(ValueError):
         orc.quantize_pack(np.zeros(128, np.float32), orc.params(4, 64, hadamard=128))    # H > B
+
+
+# ---- weight-difference quantisation (SDP4Bit README, weight quantisation) ---
+
+def test_qwd_hand_block(orc):
+    # ref = 1.0 everywhere, w = ref + HAND_X: the difference is the hand block,
+    # so codes and scale are the b=4 hand values and ref advances by s*q.
+    ref = np.ones(8, np.float32)
+    w = (ref + HAND_X).astype(np.float32)
+    codes, scales = orc.qwd_encode(w, ref, orc.params(4, 8))
+    assert int(scales[0]) == 0x3492 and codes.tobytes().hex() == "4af9851d"
+    s = 0.28564453125
+    np.testing.assert_array_equal(ref.astype(np.float64), 1.0 + np.array([2, -4, 1, 7, -3, 0, 5, -7]) * s)
+
+
+def test_qwd_receivers_track_the_sender(orc):
+    # Every receiver applying the gathered codes to its reference copy ends with
+    # the sender's reference, bit for bit, over many steps; the gap w - ref
+    # stays within half a quantum of the last step's scale (round to nearest).
+    rng = np.random.default_rng(6)
+    n, B = 8192, 2048
+    w = rng.standard_normal(n).astype(np.float32)
+    ref_send = w.copy()
+    ref_recv = w.copy()
+    p = orc.params(4, B)
+    for t in range(12):
+        w = (w - np.float32(1e-3) * rng.standard_normal(n).astype(np.float32)).astype(np.float32)
+        codes, scales = orc.qwd_encode(w, ref_send, p)
+        wout = orc.qwd_apply(codes, scales, n, p, ref_recv, w_dtype=orc.BF16)
+        np.testing.assert_array_equal(ref_send.view(np.uint32), ref_recv.view(np.uint32))
+        s = np.repeat(scales_f64(scales), B)
+        gap = np.abs(w.astype(np.float64) - ref_send.astype(np.float64))
+        assert (gap <= s / 2 + 2.0 ** -23 * np.abs(w) + 1e-30).all()
+        torch = pytest.importorskip("torch")
+        exp = torch.from_numpy(ref_recv.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        np.testing.assert_array_equal(wout, exp)
