@@ -547,6 +547,35 @@ def run_workload(args):
                  "encode_gbs": round(enc_gbs, 1), "encode_frac": round(enc_gbs / peak, 4),
                  "decode_gbs": round(dec_gbs, 1), "decode_frac": round(dec_gbs / peak, 4)}
         wl_elems = wl.n * wl.ranks
+    elif args.workload == "qwd_gpt6p7b_w8":
+        # sharded weight all-gather of a 6.7B model over 8 ranks: this rank
+        # encodes its shard's weight difference (sender), then applies all 8
+        # gathered shards to its reference copy and writes bf16 weights
+        shard = wl.n // wl.ranks
+        p = bc.QParams(wl.bits, wl.block, bc.RTN)
+        w = synth.gradients(wl.kind, shard, wl.seed, dtype=dt, **wl.params)
+        ref_shard = w.float() - 1e-3
+        ref_all = torch.zeros(wl.n, device="cuda")
+        w_all = torch.empty(wl.n, dtype=torch.bfloat16, device="cuda")
+        codes_all, scales_all = bc.alloc_codes(wl.n, p)
+        nb_shard = shard // wl.block
+        cs, ss = codes_all[: shard * wl.bits // 8], scales_all[:nb_shard]
+        def enc():
+            bc.qwd_encode(w, ref_shard, p, cs, ss)
+        def app():
+            bc.qwd_apply(codes_all, scales_all, wl.n, p, ref_all, w_all)
+        for _ in range(warm):
+            enc()
+            app()
+        te = _timed(torch, enc, K)
+        ta = _timed(torch, app, K)
+        t = te + ta
+        enc_b = shard * (2 + 4 + 4 + wl.bits / 8 + 2 / wl.block)
+        app_b = wl.n * (wl.bits / 8 + 2 / wl.block + 4 + 4 + 2)
+        algo = enc_b + app_b
+        extra = {"l2": "inputs larger than L2", "shards": wl.ranks, "weights_out": "bf16",
+                 "encode_gbs": round(enc_b / te / 1e6, 1), "encode_frac": round(enc_b / te / 1e6 / peak, 4),
+                 "apply_gbs": round(app_b / ta / 1e6, 1), "apply_frac": round(app_b / ta / 1e6 / peak, 4)}
     elif args.workload == "gpt6p7b_2bit_buckets":
         sched = bc.Scheduler(2, wl.bucket_bytes)
         x = synth.gradients(wl.kind, wl.n, wl.seed, dtype=dt, **wl.params)

@@ -12,6 +12,8 @@ The names follow the C ABI:
                                  and the all-gather (rank-ordered fp32 sum,
                                  stage-2 error feedback, requantise + repack)
   unpack_dequant                 all-gather-side decode into fp32 / bf16
+  qwd_encode, qwd_apply          weight-difference quantisation (sharded
+                                 weight all-gather)
   roundtrip                      quantise then dequantise
   Scheduler                      fusion buckets on CUDA streams
 """
@@ -103,6 +105,10 @@ def lib():
             L.bitscom_roundtrip.argtypes = [vp, st, i64, vp, P, vp, vp, vp, vp]
             L.bitscom_unpack_dequant.restype = st
             L.bitscom_unpack_dequant.argtypes = [vp, vp, i64, P, ctypes.c_float, st, vp, vp]
+            L.bitscom_qwd_encode.restype = st
+            L.bitscom_qwd_encode.argtypes = [vp, st, i64, vp, P, vp, vp, vp]
+            L.bitscom_qwd_apply.restype = st
+            L.bitscom_qwd_apply.argtypes = [vp, vp, i64, P, vp, vp, st, vp]
             L.bitscom_roundtrip_noalloc.restype = st
             L.bitscom_roundtrip_noalloc.argtypes = [vp, st, i64, vp, P, vp, vp]
             L.bitscom_roundtrip_noalloc_max_elements.restype = i64
@@ -242,6 +248,26 @@ def unpack_dequant(codes, scales, n: int, p: QParams, mul: float = 1.0, out=None
                                         ctypes.byref(p.c()), ctypes.c_float(mul), _dtype_code(out),
                                         _dev_ptr(out, "out"), _stream(stream)), "bitscom_unpack_dequant")
     return out
+
+
+def qwd_encode(w, ref, p: QParams, codes=None, scales=None, stream=None):
+    """Weight-difference encoder: codes of w - ref; ref (fp32) advances in place."""
+    n = w.numel()
+    if codes is None or scales is None:
+        codes, scales = alloc_codes(n, p, w.device)
+    _check(lib().bitscom_qwd_encode(_dev_ptr(w, "w"), _dtype_code(w), n, _dev_ptr(ref, "ref"),
+                                    ctypes.byref(p.c()), _dev_ptr(codes, "codes"), _dev_ptr(scales, "scales"),
+                                    _stream(stream)), "bitscom_qwd_encode")
+    return codes, scales
+
+
+def qwd_apply(codes, scales, n: int, p: QParams, ref, w_out=None, stream=None):
+    """Receiver update ref += s*q in place; w_out (fp32 or bf16) gets the weights."""
+    _check(lib().bitscom_qwd_apply(_dev_ptr(codes, "codes"), _dev_ptr(scales, "scales"), n,
+                                   ctypes.byref(p.c()), _dev_ptr(ref, "ref"), _dev_ptr(w_out, "w_out"),
+                                   _dtype_code(w_out) if w_out is not None else F32, _stream(stream)),
+           "bitscom_qwd_apply")
+    return w_out
 
 
 def roundtrip(x, p: QParams, err=None, codes_tmp=None, scales_tmp=None, deq_out=None, stream=None):

@@ -225,6 +225,50 @@ bitscom_status bitscom_unpack_dequant(const void* codes, const uint16_t* scales,
                                                static_cast<cudaStream_t>(cuda_stream)));
 }
 
+bitscom_status bitscom_qwd_encode(const void* w, bitscom_dtype dt, int64_t n, float* ref,
+                                  const bitscom_qparams* p, void* codes_out, uint16_t* scales_out,
+                                  void* cuda_stream)
+{
+    if (!ref && n > 0) return BITSCOM_EINVAL;
+    if (p && p->hadamard) return BITSCOM_EINVAL;
+    const bitscom_status chk = bitscom::check_encode(w, dt, n, ref, p, codes_out, scales_out);
+    if (chk != BITSCOM_OK || n == 0) return chk;
+    if (p->bits != 2 && p->bits != 4 && p->bits != 8) return BITSCOM_EUNSUPPORTED;
+    bitscom::EncArgs a;
+    a.x = w;
+    a.err = ref;
+    a.n = n;
+    a.log2B = log2_block(p->block);
+    a.nb = (n + p->block - 1) / p->block;
+    a.codes = static_cast<uint8_t*>(codes_out);
+    a.scales = scales_out;
+    a.philox_stream = p->philox_stream;
+    a.seed = p->seed;
+    a.index_offset = p->index_offset;
+    a.hadamard = 0;
+    return cuda_status(bitscom::launch_qwd_encode(a, dt == BITSCOM_F32 ? 0 : 1, p->bits,
+                                                  p->rounding == BITSCOM_SR,
+                                                  static_cast<cudaStream_t>(cuda_stream)));
+}
+
+bitscom_status bitscom_qwd_apply(const void* codes, const uint16_t* scales, int64_t n,
+                                 const bitscom_qparams* p, float* ref, void* w_out,
+                                 bitscom_dtype w_dt, void* cuda_stream)
+{
+    if (!valid_params(p) || p->hadamard || n < 0 || (w_dt != BITSCOM_F32 && w_dt != BITSCOM_BF16))
+        return BITSCOM_EINVAL;
+    if (n == 0) return BITSCOM_OK;
+    if (!codes || !scales || !ref) return BITSCOM_EINVAL;
+    if (!aligned(codes, code_align(p->bits)) || !aligned(scales, 2) || !aligned(ref, 32) ||
+        (w_out && !aligned(w_out, w_dt == BITSCOM_F32 ? 32 : 16)))
+        return BITSCOM_EALIGN;
+    if (p->bits != 2 && p->bits != 4 && p->bits != 8) return BITSCOM_EUNSUPPORTED;
+    const int wout = w_out == nullptr ? 0 : (w_dt == BITSCOM_F32 ? 1 : 2);
+    return cuda_status(bitscom::launch_qwd_apply(static_cast<const uint8_t*>(codes), scales, n,
+                                                 log2_block(p->block), ref, w_out, wout, p->bits,
+                                                 static_cast<cudaStream_t>(cuda_stream)));
+}
+
 bitscom_status bitscom_roundtrip(const void* x, bitscom_dtype dt, int64_t n, float* err,
                                  const bitscom_qparams* p, void* codes_tmp,
                                  uint16_t* scales_tmp, float* deq_out, void* cuda_stream)

@@ -71,6 +71,12 @@ inline cudaError_t launch_decode(const DecArgs& a, int bits_in, int bits_out, bo
                    : launch_decode_many(a, bits_in, bits_out, sr, st);
 }
 
+// Weight-difference quantisation: a.x = weights, a.err = reference (in/out).
+cudaError_t launch_qwd_encode(const EncArgs& a, int dtype, int bits, bool sr, cudaStream_t st);
+// wout: 0 none, 1 fp32, 2 bf16.
+cudaError_t launch_qwd_apply(const uint8_t* codes, const uint16_t* scales, int64_t n, int log2B,
+                             float* ref, void* w_out, int wout, int bits, cudaStream_t st);
+
 // out_dtype 0 = fp32, 1 = bf16.
 cudaError_t launch_dequant(const DqArgs& a, int bits, int out_dtype, cudaStream_t st);
 

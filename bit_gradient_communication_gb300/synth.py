@@ -110,6 +110,8 @@ WORKLOADS = {
                                      rounding=1, ef=True, seed=4, sr_seed=4242, bucket_bytes=25 * MiB),
     "tlq_hs_w8_gpt1p3b": Workload("tlq_hs_w8_gpt1p3b", 1_300_000_000, "bf16", "normal", {"sigma": 1e-3},
                                   bits=8, block=512, ef=True, ranks=8, ef2=True, seed=1000),
+    "qwd_gpt6p7b_w8": Workload("qwd_gpt6p7b_w8", 6_700_000_000, "bf16", "normal", {"sigma": 2e-2},
+                               bits=4, block=2048, ranks=8, seed=7),
     "allgather_decode_gpt1p3b": Workload("allgather_decode_gpt1p3b", 1_300_000_000, "bf16", "normal",
                                          {"sigma": 1e-3}, bits=4, block=128, ranks=8, seed=1000),
     "sweep_laplace_256m": Workload("sweep_laplace_256m", 268_435_456, "f32", "laplace", {"b": 1e-3},

@@ -167,6 +167,28 @@ bitscom_status bitscom_unpack_dequant(const void* codes, const uint16_t* scales,
                                       void* out, void* cuda_stream);
 
 /*
+ * Weight-difference quantisation for the sharded weight all-gather (SDP4Bit
+ * README, "Weight Quantization Arguments": --quantized-weights,
+ * --weight-quantization-bits 4, --wq-group-size 2048; "quantization on weight
+ * differences").  The shard owner quantises d = fl(w - ref) against the
+ * reference copy every rank holds and advances its own copy:
+ * ref = fl(ref + fl(s*q)); every rank then applies the all-gathered codes to
+ * its copy with bitscom_qwd_apply, so all copies stay bit-identical and the
+ * residual w - ref carries into the next step.  Bits 2, 4, 8; no Hadamard.
+ *   w          [n] weights, fp32 (32-byte aligned) or bf16 (16-byte aligned).
+ *   ref        [n] fp32 reference, in/out (32-byte aligned).
+ *   codes_out, scales_out   as in bitscom_quantize_pack.
+ */
+bitscom_status bitscom_qwd_encode(const void* w, bitscom_dtype dt, int64_t n, float* ref,
+                                  const bitscom_qparams* p, void* codes_out, uint16_t* scales_out,
+                                  void* cuda_stream);
+/* Receiver side: ref = fl(ref + fl(s*q)) for n elements of gathered codes;
+ * w_out (NULL = none) receives the new weights as fp32 or bf16 (w_dt). */
+bitscom_status bitscom_qwd_apply(const void* codes, const uint16_t* scales, int64_t n,
+                                 const bitscom_qparams* p, float* ref, void* w_out,
+                                 bitscom_dtype w_dt, void* cuda_stream);
+
+/*
  * Quantise then dequantise (the simulate_quantization mode of "Implemented
  * Features"): the encoder into caller scratch codes_tmp / scales_tmp, then the
  * single-rank decoder into deq_out.  deq_out may alias x when dt == F32.

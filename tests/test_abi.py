@@ -195,3 +195,19 @@ def test_hadamard_argument_checks(bc):
         ctypes.byref(bc.QParams(4, 128, hadamard=128).c()), None, None,
         ctypes.byref(bc.QParams(4, 128).c()), _fake(0x20000), _fake(0x30000), None)
     assert st == 1
+
+
+def test_qwd_argument_checks(bc):
+    L = bc.lib()
+    q = bc.QParams(4, 2048).c()
+    assert L.bitscom_qwd_encode(_fake(0x10000), 0, 4096, None, ctypes.byref(q), _fake(0x20000),
+                                _fake(0x30000), None) == 1          # reference required
+    qh = bc.QParams(4, 128, hadamard=128).c()
+    assert L.bitscom_qwd_encode(_fake(0x10000), 0, 4096, _fake(0x40000), ctypes.byref(qh), _fake(0x20000),
+                                _fake(0x30000), None) == 1          # no rotation for weights
+    q12 = bc.QParams(12, 2048).c()
+    assert L.bitscom_qwd_encode(_fake(0x10000), 0, 4096, _fake(0x40000), ctypes.byref(q12),
+                                _fake(0x20000), _fake(0x30000), None) == 3
+    assert L.bitscom_qwd_apply(_fake(0x20000), _fake(0x30000), 4096, ctypes.byref(q), _fake(0x40004),
+                               None, 0, None) == 2                  # reference alignment
+    assert L.bitscom_qwd_apply(_fake(0x20000), _fake(0x30000), 0, ctypes.byref(q), None, None, 0, None) == 0

@@ -301,3 +301,37 @@ def test_hadamard_roundtrip_matches_oracle():
     _, _, d_ref = O.roundtrip(x, O.params(4, 128, hadamard=128), e_ref)
     assert np.array_equal(deq.cpu().numpy().view(np.uint32), d_ref.view(np.uint32))
     assert np.array_equal(eg.cpu().numpy().view(np.uint32), e_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("block,rounding", [(2048, 0), (128, 1), (8, 0)])
+def test_qwd_matches_oracle_over_steps(dt, bits, block, rounding):
+    # Weight-difference quantisation: the sender's encoder (ref advances) and a
+    # receiver's apply (ref advances, bf16 weights out), three steps in a row.
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(bits * 10 + block)
+    n = 3 * 4096 + 2 * block + 8
+    w = rng.standard_normal(n).astype(np.float32)
+    ref_s = torch.from_numpy(w.copy()).cuda()
+    ref_r = torch.from_numpy(w.copy()).cuda()
+    h_ref_s, h_ref_r = w.copy(), w.copy()
+    for t in range(3):
+        w = (w + np.float32(1e-3) * rng.standard_normal(n).astype(np.float32)).astype(np.float32)
+        wh = w if dt == "f32" else bf16_bits_of(torch, w)
+        wg = torch.from_numpy(wh if dt == "f32" else wh.view(np.int16)).cuda()
+        if dt == "bf16":
+            wg = wg.view(torch.bfloat16)
+        p = bc.QParams(bits, block, rounding, seed=9, index_offset=t * n)
+        po = O.params(bits, block, rounding, seed=9, index_offset=t * n)
+        codes, scales = bc.qwd_encode(wg, ref_s, p)
+        wout = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+        bc.qwd_apply(codes, scales, n, p, ref_r, wout)
+        torch.cuda.synchronize()
+        c_ref, s_ref = O.qwd_encode(wh, h_ref_s, po)
+        w_ref = O.qwd_apply(c_ref, s_ref, n, po, h_ref_r, O.BF16)
+        assert codes.cpu().numpy().tobytes() == c_ref.tobytes(), f"step {t}"
+        assert np.array_equal(scales.cpu().numpy().view(np.uint16), s_ref), f"step {t}"
+        assert np.array_equal(ref_s.cpu().numpy().view(np.uint32), h_ref_s.view(np.uint32)), f"step {t}"
+        assert np.array_equal(ref_r.cpu().numpy().view(np.uint32), h_ref_r.view(np.uint32)), f"step {t}"
+        assert np.array_equal(wout.view(torch.int16).cpu().numpy().view(np.uint16), w_ref), f"step {t}"
