@@ -551,19 +551,24 @@ def run_workload(args):
         # sharded weight all-gather of a 6.7B model over 8 ranks: this rank
         # encodes its shard's weight difference (sender), then applies all 8
         # gathered shards to its reference copy and writes bf16 weights
-        shard = wl.n // wl.ranks
+        # shards padded to whole groups, so every shard starts on a group boundary
+        shard = (wl.n // wl.ranks + wl.block - 1) // wl.block * wl.block
+        n_all = shard * wl.ranks
         p = bc.QParams(wl.bits, wl.block, bc.RTN)
         w = synth.gradients(wl.kind, shard, wl.seed, dtype=dt, **wl.params)
         ref_shard = w.float() - 1e-3
-        ref_all = torch.zeros(wl.n, device="cuda")
-        w_all = torch.empty(wl.n, dtype=torch.bfloat16, device="cuda")
-        codes_all, scales_all = bc.alloc_codes(wl.n, p)
+        ref_all = torch.zeros(n_all, device="cuda")
+        w_all = torch.empty(n_all, dtype=torch.bfloat16, device="cuda")
+        codes_all, scales_all = bc.alloc_codes(n_all, p)
         nb_shard = shard // wl.block
         cs, ss = codes_all[: shard * wl.bits // 8], scales_all[:nb_shard]
         def enc():
             bc.qwd_encode(w, ref_shard, p, cs, ss)
         def app():
-            bc.qwd_apply(codes_all, scales_all, wl.n, p, ref_all, w_all)
+            bc.qwd_apply(codes_all, scales_all, n_all, p, ref_all, w_all)
+        for r in range(wl.ranks):       # every shard's codes, as if gathered from its owner
+            bc.qwd_encode(w, ref_shard.clone(), p, codes_all[r * shard * wl.bits // 8:(r + 1) * shard * wl.bits // 8],
+                          scales_all[r * nb_shard:(r + 1) * nb_shard])
         for _ in range(warm):
             enc()
             app()
@@ -571,9 +576,9 @@ def run_workload(args):
         ta = _timed(torch, app, K)
         t = te + ta
         enc_b = shard * (2 + 4 + 4 + wl.bits / 8 + 2 / wl.block)
-        app_b = wl.n * (wl.bits / 8 + 2 / wl.block + 4 + 4 + 2)
+        app_b = n_all * (wl.bits / 8 + 2 / wl.block + 4 + 4 + 2)
         algo = enc_b + app_b
-        extra = {"l2": "inputs larger than L2", "shards": wl.ranks, "weights_out": "bf16",
+        extra = {"l2": "inputs larger than L2", "shards": wl.ranks, "shard_elems": shard, "weights_out": "bf16",
                  "encode_gbs": round(enc_b / te / 1e6, 1), "encode_frac": round(enc_b / te / 1e6 / peak, 4),
                  "apply_gbs": round(app_b / ta / 1e6, 1), "apply_frac": round(app_b / ta / 1e6 / peak, 4)}
     elif args.workload == "gpt6p7b_2bit_buckets":
