@@ -335,3 +335,29 @@ def test_qwd_matches_oracle_over_steps(dt, bits, block, rounding):
         assert np.array_equal(ref_s.cpu().numpy().view(np.uint32), h_ref_s.view(np.uint32)), f"step {t}"
         assert np.array_equal(ref_r.cpu().numpy().view(np.uint32), h_ref_r.view(np.uint32)), f"step {t}"
         assert np.array_equal(wout.view(torch.int16).cpu().numpy().view(np.uint16), w_ref), f"step {t}"
+
+
+@pytest.mark.parametrize("bits", [2, 4, 16])
+def test_decoder_maximum_ranks(bits):
+    # W = 64, the largest rank count the ABI accepts (eight groups of eight in
+    # the many-rank kernel), with requantisation and stage-2 error feedback.
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(64 + bits)
+    n, W, B = 2 * 4096 + 72, 64, 128
+    ins = [_random_codes(rng, n, bits, B) for _ in range(W)]
+    cin = [torch.from_numpy(c).cuda() for c, _ in ins]
+    sin = [torch.from_numpy(s.view(np.int16)).cuda() for _, s in ins]
+    e2 = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    e2g = torch.from_numpy(e2.copy()).cuda()
+    p = bc.QParams(bits, B, bc.SR, seed=3, philox_stream=1)
+    sum_, co, so = bc.unpack_dequant_reduce_requant(cin, sin, n, bc.QParams(bits, B), sum_out=True, err2=e2g,
+                                                    p_out=p)
+    torch.cuda.synchronize()
+    e2_ref = e2.copy()
+    s_ref, c_ref, sc_ref = O.unpack_dequant_reduce_requant(
+        [c for c, _ in ins], [s for _, s in ins], n, O.params(bits, B), True, e2_ref,
+        O.params(bits, B, O.SR, seed=3, philox_stream=1))
+    assert np.array_equal(sum_.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert co.cpu().numpy().tobytes() == c_ref.tobytes()
+    assert np.array_equal(so.cpu().numpy().view(np.uint16), sc_ref)
+    assert np.array_equal(e2g.cpu().numpy().view(np.uint32), e2_ref.view(np.uint32))
