@@ -448,9 +448,15 @@ def run_workload(args):
     if args.workload == "sweep_laplace_256m":
         x = synth.gradients(wl.kind, wl.n, wl.seed, **wl.params)
         deq = torch.empty(wl.n, device="cuda")
+        only = None
+        if args.sweep_filter:
+            fb, fB, fr = args.sweep_filter.split(",")
+            only = (int(fb), int(fB), bc.SR if fr == "sr" else bc.RTN)
         for bits in (1, 2, 4, 8, 12, 16):
             for block in (32, 64, 128, 256, 1024, 4096):
                 for rounding in (bc.RTN, bc.SR):
+                    if only and (bits, block, rounding) != only:
+                        continue
                     p = bc.QParams(bits, block, rounding, seed=wl.sr_seed)
                     codes, scales = bc.alloc_codes(wl.n, p)
                     enc = lambda: bc.quantize_pack(x, p, None, codes, scales)
@@ -468,7 +474,8 @@ def run_workload(args):
                                   "encode_input_gbs": round(wl.n * 4 / te / 1e6, 1)})
                     del codes, scales
         best = max(lines, key=lambda r: r["encode_input_gbs"])
-        head = next(r for r in lines if r["bits"] == 4 and r["block"] == 128 and r["rounding"] == "rtn")
+        head = next((r for r in lines if r["bits"] == 4 and r["block"] == 128 and r["rounding"] == "rtn"),
+                    lines[0])
         out = {"metric": METRIC, "value": head["encode_input_gbs"], "unit": UNIT, "n_gpus": 1, "steps": K,
                "warmup": warm, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
                "config": {"workload": wl.name, "n": wl.n, "input_dtype": "f32",
@@ -618,6 +625,8 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=1 << 21)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep-filter", default=None,
+                    help="bits,block,rtn|sr: run one configuration of sweep_laplace_256m")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="another workload recipe from synth.WORKLOADS (one JSON line of its own)")
     args = ap.parse_args()

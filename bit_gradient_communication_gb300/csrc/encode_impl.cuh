@@ -56,8 +56,9 @@ __device__ __forceinline__ void load_row(const EncArgs& a, int64_t row, RowIn<IN
 
 // IN: 0 = fp32, 1 = bf16.  HAD: rotate every a.hadamard-element block of g by
 // the Walsh-Hadamard transform before the error is added.  The row loop is
-// software-pipelined: the loads of row r + gridDim.x are issued before row r
-// is computed.
+// software-pipelined: the loads of row r + gridDim.x (with error feedback) or
+// of row r + 2 gridDim.x (without: two buffers, the loop unrolled by two) are
+// issued before row r is computed.
 template <int IN, int BITS, bool EF, bool SR, bool HAD>
 __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
 {
@@ -68,11 +69,10 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
     const int64_t padded = a.nb << a.log2B;
     const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
     const uint32_t shift = (uint32_t)(a.index_offset & 3u);
-    int parity = 0;
+    const int64_t G = gridDim.x;
 
-    RowIn<IN, EF> cur;
-    if ((int64_t)blockIdx.x < rows) load_row<IN, EF>(a, blockIdx.x, cur);
-    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
+    // One row: `cur` holds its inputs and is refilled with row `ahead`.
+    auto process = [&](RowIn<IN, EF>& cur, int64_t row, int64_t ahead, int parity) {
         const int64_t e0 = row * kRow + (int64_t)threadIdx.x * kPiece;
         const int64_t piece = e0 >> 3;
         const int64_t rem = n - e0;
@@ -89,8 +89,8 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
 #pragma unroll
             for (int j = 0; j < 8; ++j) v[j] = __fadd_rn(v[j], cur.e[j]);
         }
-        // prefetch: the next row's loads overlap this row's arithmetic
-        if (row + gridDim.x < rows) load_row<IN, EF>(a, row + gridDim.x, cur);
+        // prefetch: row `ahead` reuses this buffer; its loads overlap the arithmetic
+        if (ahead < rows) load_row<IN, EF>(a, ahead, cur);
 
         // block statistic: absmax (b >= 2) or tree sum of |v| (b = 1)
         float stat;
@@ -136,6 +136,21 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) if (j < valid) a.err[e0 + j] = e[j];
             }
+        }
+    };
+
+    if constexpr (EF) {
+        RowIn<IN, EF> cur;
+        if ((int64_t)blockIdx.x < rows) load_row<IN, EF>(a, blockIdx.x, cur);
+        int parity = 0;
+        for (int64_t row = blockIdx.x; row < rows; row += G, parity ^= 1) process(cur, row, row + G, parity);
+    } else {
+        RowIn<IN, EF> A, B;
+        if ((int64_t)blockIdx.x < rows) load_row<IN, EF>(a, blockIdx.x, A);
+        if ((int64_t)blockIdx.x + G < rows) load_row<IN, EF>(a, blockIdx.x + G, B);
+        for (int64_t row = blockIdx.x; row < rows; row += 2 * G) {
+            process(A, row, row + 2 * G, 0);
+            if (row + G < rows) process(B, row + G, row + 3 * G, 1);
         }
     }
 }
