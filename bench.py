@@ -162,17 +162,23 @@ class AllReduceW8:
                               stream=stream)
 
     def decode(self, stream=None):
+        for c in range(len(self.chunks)):
+            self.decode_chunk(c, stream)
+
+    def decode_chunk(self, c, stream=None):
+        """Chunk c's decoder: the W ranks' codes of chunk c (what the all-to-all
+        delivers to rank c), summed, requantised into chunk c of the output."""
+        lo, hi = self.chunks[c]
         b1, B1 = self.p1[0].bits, self.p1[0].block
         b2, B2 = self.p2.bits, self.p2.block
-        for lo, hi in self.chunks:
-            hi1 = (hi + B1 - 1) // B1 * B1
-            hi2 = (hi + B2 - 1) // B2 * B2
-            cin = [c[lo * b1 // 8: hi1 * b1 // 8] for c in self.codes]
-            sin = [s[lo // B1: hi1 // B1] for s in self.scales]
-            self.bc.unpack_dequant_reduce_requant(
-                cin, sin, hi - lo, self.p1[0], sum_out=None, err2=self.err2[lo:hi],
-                p_out=self.p2.shifted(lo), codes_out=self.codes_out[lo * b2 // 8: hi2 * b2 // 8],
-                scales_out=self.scales_out[lo // B2: hi2 // B2], stream=stream)
+        hi1 = (hi + B1 - 1) // B1 * B1
+        hi2 = (hi + B2 - 1) // B2 * B2
+        cin = [x[lo * b1 // 8: hi1 * b1 // 8] for x in self.codes]
+        sin = [x[lo // B1: hi1 // B1] for x in self.scales]
+        self.bc.unpack_dequant_reduce_requant(
+            cin, sin, hi - lo, self.p1[0], sum_out=None, err2=self.err2[lo:hi],
+            p_out=self.p2.shifted(lo), codes_out=self.codes_out[lo * b2 // 8: hi2 * b2 // 8],
+            scales_out=self.scales_out[lo // B2: hi2 // B2], stream=stream)
 
 
 def run_ours(args, rank, world, local_rank):
@@ -291,7 +297,8 @@ def run_e2e(torch, bc, ar, args, dev):
     """Host -> device copies of the 8 ranks' gradients (pinned), the step, and
     the requantised codes + scales back to the host, all inside the timed
     region.  Rank w's copy runs on a copy stream and overlaps rank w-1's
-    encoder."""
+    encoder; chunk c's result goes back on a second copy stream as soon as
+    chunk c's decoder has finished."""
     W, n = ar.W, ar.n
     host_x = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(W)]
     for w in range(W):
@@ -299,25 +306,36 @@ def run_e2e(torch, bc, ar, args, dev):
     host_codes = torch.empty(ar.codes_out.numel(), dtype=torch.uint8, pin_memory=True)
     host_scales = torch.empty(ar.scales_out.numel(), dtype=torch.int16, pin_memory=True)
     compute = torch.cuda.current_stream()
-    copy = torch.cuda.Stream(device=dev)
+    h2d_stream = torch.cuda.Stream(device=dev)
+    d2h_stream = torch.cuda.Stream(device=dev)
     h2d = sum(t.numel() * t.element_size() for t in host_x)
     d2h = host_codes.numel() + host_scales.numel() * 2
+    b2, B2 = ar.p2.bits, ar.p2.block
 
     def step():
+        h2d_stream.wait_stream(compute)         # the previous step has consumed x
         done = []
         for w in range(W):
-            copy.wait_stream(compute) if w == 0 else None
-            with torch.cuda.stream(copy):
+            with torch.cuda.stream(h2d_stream):
                 ar.x[w].copy_(host_x[w], non_blocking=True)
                 e = torch.cuda.Event()
-                e.record(copy)
+                e.record(h2d_stream)
             done.append(e)
         for w in range(W):
             compute.wait_event(done[w])
             ar.encode_rank(w)
-        ar.decode()
-        host_codes.copy_(ar.codes_out, non_blocking=True)
-        host_scales.copy_(ar.scales_out, non_blocking=True)
+        d2h_stream.wait_stream(compute)
+        for c, (lo, hi) in enumerate(ar.chunks):
+            ar.decode_chunk(c)
+            ev = torch.cuda.Event()
+            ev.record(compute)
+            d2h_stream.wait_event(ev)
+            hi2 = (hi + B2 - 1) // B2 * B2
+            with torch.cuda.stream(d2h_stream):
+                host_codes[lo * b2 // 8: hi2 * b2 // 8].copy_(ar.codes_out[lo * b2 // 8: hi2 * b2 // 8],
+                                                              non_blocking=True)
+                host_scales[lo // B2: hi2 // B2].copy_(ar.scales_out[lo // B2: hi2 // B2], non_blocking=True)
+        compute.wait_stream(d2h_stream)
 
     steps = max(1, min(args.steps, args.e2e_steps))
     for _ in range(2):

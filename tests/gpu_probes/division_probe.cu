@@ -69,7 +69,68 @@ __global__ void probe(uint32_t n_v, unsigned long long* bad, uint32_t* first)
     }
 }
 
+// RN(1/s) of every positive finite fp16 value against __frcp_rn.
+__global__ void recip_probe(unsigned long long* bad, uint32_t* first)
+{
+    const uint32_t h = 1u + blockIdx.x * blockDim.x + threadIdx.x;
+    if (h > kMaxScale) return;
+    const float s = __half2float(__ushort_as_half((unsigned short)h));
+    const float got = bitscom::scale_reciprocal(s), ref = __frcp_rn(s);
+    if (__float_as_uint(got) != __float_as_uint(ref)) {
+        const unsigned long long slot = atomicAdd(bad, 1ull);
+        if (slot < kSlots) { first[3 * slot] = h; first[3 * slot + 1] = __float_as_uint(got); first[3 * slot + 2] = __float_as_uint(ref); }
+    }
+}
+
+// The fp16 block scale from every fp32 absmax bit pattern in [lo, hi) against
+// fp16_rne(min(__fdiv_rn(absmax, Qmax), 65504)), and the fp32 quotient itself
+// against __fdiv_rn.
+template <int BITS>
+__global__ void scale_probe(uint32_t lo, uint32_t hi, unsigned long long* bad, uint32_t* first)
+{
+    constexpr float Q = (float)((1 << (BITS - 1)) - 1);
+    constexpr float yQ = (float)(1.0 / (double)((1 << (BITS - 1)) - 1));
+    for (uint64_t u = lo + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; u < hi;
+         u += (uint64_t)gridDim.x * blockDim.x) {
+        const float stat = __uint_as_float((uint32_t)u);
+        const __half got = bitscom::block_scale<BITS>(stat, 8);
+        const __half ref = __float2half_rn(fminf(__fdiv_rn(stat, Q), 65504.0f));
+        const bool q_ok = __float_as_uint(bitscom::div_by_scale(stat, Q, yQ)) == __float_as_uint(__fdiv_rn(stat, Q));
+        if (__half_as_ushort(got) != __half_as_ushort(ref) || !q_ok) {
+            const unsigned long long slot = atomicAdd(bad, 1ull);
+            if (slot < kSlots) { first[3 * slot] = (uint32_t)u; first[3 * slot + 1] = BITS; first[3 * slot + 2] = __half_as_ushort(got); }
+        }
+    }
+}
+
 }  // namespace
+
+// which: 0 = reciprocal of every fp16 scale, 1 = block scale over [2^-100, 2^100).
+extern "C" int run_scale_probe(int which, unsigned long long* bad_out, uint32_t* first_out)
+{
+    unsigned long long* bad = nullptr;
+    uint32_t* first = nullptr;
+    if (cudaMalloc(&bad, sizeof(*bad)) != cudaSuccess) return 1;
+    if (cudaMalloc(&first, 3 * kSlots * sizeof(uint32_t)) != cudaSuccess) return 2;
+    cudaMemset(bad, 0, sizeof(*bad));
+    cudaMemset(first, 0, 3 * kSlots * sizeof(uint32_t));
+    if (which == 0) {
+        recip_probe<<<(kMaxScale + 255) / 256, 256>>>(bad, first);
+    } else {
+        const uint32_t lo = 0x0D800000u, hi = 0x71800000u;   // [2^-100, 2^100)
+        scale_probe<2><<<4096, 512>>>(lo, hi, bad, first);
+        scale_probe<4><<<4096, 512>>>(lo, hi, bad, first);
+        scale_probe<8><<<4096, 512>>>(lo, hi, bad, first);
+        scale_probe<12><<<4096, 512>>>(lo, hi, bad, first);
+        scale_probe<16><<<4096, 512>>>(lo, hi, bad, first);
+    }
+    int rc = cudaDeviceSynchronize() == cudaSuccess ? 0 : 3;
+    cudaMemcpy(bad_out, bad, sizeof(*bad), cudaMemcpyDeviceToHost);
+    cudaMemcpy(first_out, first, 3 * kSlots * sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    cudaFree(bad);
+    cudaFree(first);
+    return rc;
+}
 
 extern "C" int run_division_probe(uint32_t n_v, unsigned long long* bad_out, uint32_t* first_out)
 {
