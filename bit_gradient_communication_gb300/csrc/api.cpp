@@ -176,6 +176,19 @@ bitscom_status bitscom_unpack_dequant_reduce_requant(
     const bitscom_status chk = bitscom::check_decode(codes_in, scales_in, W, n, p_in, sum_out, err2,
                                                      p_out, codes_out, scales_out);
     if (chk != BITSCOM_OK || n == 0) return chk;
+    if (W == 1 && !p_out && p_in->hadamard == 0) {
+        // one rank, no requantisation: the sum is fl(s*q) itself, which the
+        // all-gather-side decode kernel writes with mul = 1 (fl(d * 1) = d)
+        bitscom::DqArgs d;
+        d.codes = static_cast<const uint8_t*>(codes_in[0]);
+        d.scales = scales_in[0];
+        d.n = n;
+        d.log2B = log2_block(p_in->block);
+        d.mul = 1.0f;
+        d.out = sum_out;
+        d.hadamard = 0;
+        return cuda_status(bitscom::launch_dequant(d, p_in->bits, 0, static_cast<cudaStream_t>(cuda_stream)));
+    }
     bitscom::DecArgs a;
     std::memset(&a, 0, sizeof(a));
     for (int w = 0; w < W; ++w) {
