@@ -159,8 +159,7 @@ bitscom_status bitscom_quantize_pack(const void* x, bitscom_dtype dt, int64_t n,
     a.nb = (n + p->block - 1) / p->block;
     a.codes = static_cast<uint8_t*>(codes_out);
     a.scales = scales_out;
-    a.philox_stream = p->philox_stream;
-    a.seed = p->seed;
+    a.keys = bitscom::philox_keys(p->seed, p->philox_stream);
     a.index_offset = p->index_offset;
     a.hadamard = p->hadamard;
     return cuda_status(bitscom::launch_encode(a, dt == BITSCOM_F32 ? 0 : 1, p->bits,
@@ -205,8 +204,7 @@ bitscom_status bitscom_unpack_dequant_reduce_requant(
     a.codes_out = static_cast<uint8_t*>(codes_out);
     a.scales_out = scales_out;
     if (p_out) {
-        a.philox_stream = p_out->philox_stream;
-        a.seed = p_out->seed;
+        a.keys = bitscom::philox_keys(p_out->seed, p_out->philox_stream);
         a.index_offset = p_out->index_offset;
     }
     return cuda_status(bitscom::launch_decode(a, p_in->bits, p_out ? p_out->bits : 0,
@@ -255,8 +253,7 @@ bitscom_status bitscom_qwd_encode(const void* w, bitscom_dtype dt, int64_t n, fl
     a.nb = (n + p->block - 1) / p->block;
     a.codes = static_cast<uint8_t*>(codes_out);
     a.scales = scales_out;
-    a.philox_stream = p->philox_stream;
-    a.seed = p->seed;
+    a.keys = bitscom::philox_keys(p->seed, p->philox_stream);
     a.index_offset = p->index_offset;
     a.hadamard = 0;
     return cuda_status(bitscom::launch_qwd_encode(a, dt == BITSCOM_F32 ? 0 : 1, p->bits,

@@ -184,8 +184,7 @@ decode_kernel(const DecArgs a)
 
             uint32_t rw[8];
             if constexpr (SR && BOUT > 1) {
-                random_words8(a.index_offset + (uint64_t)e0, a.philox_stream, (uint32_t)a.seed,
-                              (uint32_t)(a.seed >> 32), (uint32_t)(a.index_offset & 3u), rw);
+                random_words8(a.index_offset + (uint64_t)e0, a.keys, (uint32_t)(a.index_offset & 3u), rw);
             } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) rw[j] = 0u;

@@ -9,6 +9,38 @@
 
 namespace bitscom {
 
+// Philox4x32-10 multipliers and Weyl constants (Salmon, Moraes, Dror, Shaw,
+// "Parallel random numbers: as easy as 1, 2, 3", SC'11).
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u, kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u, kPhiloxW1 = 0xBB67AE85u;
+
+// The key schedule of one launch, expanded on the host so that the kernels
+// take every round key from the parameter bank.  Round r uses the key
+// (k0 + r W0, k1 + r W1) mod 2^32.  Counter words 2 and 3 are the same for
+// every element of a launch (the Philox stream and 0), so the second product
+// of round 0 is a launch constant too and is folded into the two x-terms it
+// feeds: x0 = hi(M1 stream) ^ k0 (round 0) and x1 = lo(M1 stream) ^ (k0 + W0)
+// (round 1).
+struct PhiloxKeys {
+    uint32_t x0, x1;
+    uint32_t k0[10];        // k0 + r W0; rounds 2..9 read it
+    uint32_t k1[10];        // k1 + r W1
+};
+
+inline PhiloxKeys philox_keys(uint64_t seed, uint32_t stream)
+{
+    PhiloxKeys k;
+    const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        k.k0[r] = key0 + (uint32_t)r * kPhiloxW0;
+        k.k1[r] = key1 + (uint32_t)r * kPhiloxW1;
+    }
+    const uint64_t p1 = (uint64_t)kPhiloxM1 * stream;
+    k.x0 = (uint32_t)(p1 >> 32) ^ k.k0[0];
+    k.x1 = (uint32_t)p1 ^ k.k0[1];
+    return k;
+}
+
 struct EncArgs {
     const void* x;          // fp32 or bf16 [n]
     float* err;             // [n] or nullptr
@@ -17,8 +49,7 @@ struct EncArgs {
     uint8_t* codes;         // packed_bytes(n)
     uint16_t* scales;       // [nb]
     int log2B;
-    uint32_t philox_stream;
-    uint64_t seed;
+    PhiloxKeys keys;        // stochastic rounding: philox_keys(seed, stream)
     uint64_t index_offset;
     int hadamard;           // 0 or the transform block H
 };
@@ -37,8 +68,7 @@ struct DecArgs {
     float* err2;            // [n] or nullptr
     uint8_t* codes_out;     // or nullptr (no requantisation)
     uint16_t* scales_out;
-    uint32_t philox_stream;
-    uint64_t seed;
+    PhiloxKeys keys;        // stochastic requantisation: philox_keys(seed, stream)
     uint64_t index_offset;
 };
 

@@ -28,7 +28,6 @@ __global__ void __launch_bounds__(kThreads, 2) qwd_encode_kernel(const EncArgs a
     const int64_t n = a.n;
     const int64_t rows = (n + kRow - 1) / kRow;
     const int64_t padded = a.nb << a.log2B;
-    const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
     const uint32_t shift = (uint32_t)(a.index_offset & 3u);
     float* ref = a.err;
     int parity = 0;
@@ -62,7 +61,7 @@ __global__ void __launch_bounds__(kThreads, 2) qwd_encode_kernel(const EncArgs a
         const float s = __half2float(sh);
         uint32_t rw[8];
         if constexpr (SR) {
-            random_words8(a.index_offset + (uint64_t)e0, a.philox_stream, k0, k1, shift, rw);
+            random_words8(a.index_offset + (uint64_t)e0, a.keys, shift, rw);
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) rw[j] = 0u;

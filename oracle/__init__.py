@@ -86,6 +86,8 @@ def lib():
             L.orc_philox4x32_10.argtypes = [vp, vp, vp]
             L.orc_random_word.restype = u32
             L.orc_random_word.argtypes = [u64, u32, u64]
+            L.orc_random_words.restype = None
+            L.orc_random_words.argtypes = [u64, u32, u64, ctypes.c_int64, ctypes.c_void_p]
             L.orc_quantize_pack.restype = ctypes.c_int
             L.orc_quantize_pack.argtypes = [vp, i32, i64, vp, P, vp, vp]
             L.orc_unpack_dequant_reduce_requant.restype = ctypes.c_int
@@ -145,6 +147,12 @@ def philox4x32_10(ctr, key):
 
 def random_word(seed, stream, i):
     return lib().orc_random_word(seed, stream, i)
+
+
+def random_words(seed, stream, i0, n):
+    out = np.zeros(n, dtype=np.uint32)
+    lib().orc_random_words(seed, stream, i0, n, _ptr(out))
+    return out
 
 
 # ---- codec ----------------------------------------------------------------

@@ -146,6 +146,11 @@ uint32_t orc_random_word(uint64_t seed, uint32_t stream, uint64_t i)
     return out[i & 3];
 }
 
+void orc_random_words(uint64_t seed, uint32_t stream, uint64_t i0, int64_t n, uint32_t* out)
+{
+    for (int64_t k = 0; k < n; ++k) out[k] = orc_random_word(seed, stream, i0 + (uint64_t)k);
+}
+
 /* ------------------------------------------------------------------ */
 /* Scalar rules                                                         */
 /* ------------------------------------------------------------------ */

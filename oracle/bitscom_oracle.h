@@ -48,6 +48,8 @@ void     orc_f32_to_f16_many(const float* x, uint16_t* out, int64_t n);
 void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
 /* The 32-bit random word the codec draws for global element index i. */
 uint32_t orc_random_word(uint64_t seed, uint32_t stream, uint64_t i);
+/* The words of elements i0 .. i0+n-1, one orc_random_word call each (a test helper). */
+void orc_random_words(uint64_t seed, uint32_t stream, uint64_t i0, int64_t n, uint32_t* out);
 
 /* Encoder.  dtype 0 = fp32, 1 = bf16 (raw uint16 bits).  err may be NULL
  * (no error feedback).  codes receives packed_bytes(n) bytes, scales

@@ -16,6 +16,7 @@ from gpu_util import need_gpu
 pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(os.path.dirname(HERE), "bit_gradient_communication_gb300", "csrc")
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 
 @pytest.fixture(scope="module")
@@ -24,7 +25,7 @@ def probe(tmp_path_factory):
     so = tmp_path_factory.mktemp("probe") / "division_probe.so"
     nvcc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
     subprocess.check_call([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
-                           "-fmad=false", "-Xcompiler", "-fPIC", "-shared", "-I", CSRC,
+                           "-fmad=false", "-Xcompiler", "-fPIC", "-shared", "-I", CSRC, "-I", INCLUDE,
                            os.path.join(HERE, "gpu_probes", "division_probe.cu"), "-o", str(so)])
     return ctypes.CDLL(str(so))
 

@@ -103,6 +103,53 @@ def test_encoder_special_blocks():
                 assert np.array_equal(err.view(np.uint32), e_ref.view(np.uint32))
 
 
+def _zero_fraction_indices(seed, count=3):
+    """Global indices whose Philox word has zero low 23 bits (u = 0), found
+    with the oracle's generator: there a positive t however small rounds up."""
+    words = O.random_words(seed, 0, 0, 1 << 24)
+    hits = np.nonzero((words & 0x7FFFFF) == 0)[0]
+    assert hits.size >= count
+    return [int(h) for h in hits[:count]]
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8, 12, 16])
+@pytest.mark.parametrize("absmax", [10.5, 14.0, 21.0])
+def test_encoder_sr_tiny_elements(bits, absmax):
+    # Stochastic rounding of elements whose quotient t = v/s is tiny or
+    # subnormal, placed where u = 0 so that only t > 0 decides q = 1; v/s near
+    # the bottom of the subnormal range (2^-149 / s for s around 1.5 .. 3)
+    # rounds to 0 or to 2^-149 by IEEE division.  Also -0, +0, the 2^-96
+    # boundary and a block whose scale underflows.
+    torch, bc = need_gpu()
+    seed = 11
+    n = 4096
+    rng = np.random.default_rng(bits * 13 + int(absmax))
+    specials = [2.0 ** -149, -2.0 ** -149, 3 * 2.0 ** -149, 2.0 ** -100, -2.0 ** -97, 2.0 ** -96,
+                -2.0 ** -96, 0.0, -0.0, 1.5 * 2.0 ** -126, 2.0 ** -130]
+    for h in _zero_fraction_indices(seed):
+        for pos in (200, 203):                       # 203: index offset not a multiple of 4
+            for tiny in specials[:4]:
+                x = (rng.standard_normal(n) * absmax / 8).astype(np.float32)
+                x[128:256] = np.clip(x[128:256], -absmax / 2, absmax / 2)
+                x[130] = absmax
+                x[pos] = tiny
+                x[pos + 1:pos + 1 + len(specials)] = specials
+                x[1024:1152] = 2.0 ** -140           # scale underflows to 0
+                x[1030] = 2.0 ** -149
+                p = bc.QParams(bits, 128, bc.SR, seed=seed, index_offset=h - pos)
+                for ef in (False, True):
+                    e = np.zeros(n, np.float32)
+                    codes, scales, err = _run_encode(torch, bc, x, "f32", n, p, e.copy() if ef else None)
+                    e_ref = e.copy() if ef else None
+                    c_ref, s_ref = O.quantize_pack(x, O.params(bits, 128, O.SR, seed=seed, index_offset=h - pos),
+                                                   e_ref)
+                    tag = f"h={h} pos={pos} tiny={tiny} ef={ef}"
+                    assert codes.tobytes() == c_ref.tobytes(), tag
+                    assert np.array_equal(scales, s_ref), tag
+                    if ef:
+                        assert np.array_equal(err.view(np.uint32), e_ref.view(np.uint32)), tag
+
+
 def _random_codes(rng, n, bits, block, scale_sigma=1e-3):
     nbytes = O.packed_bytes(n, bits, block)
     codes = rng.integers(0, 256, nbytes, dtype=np.uint8)

@@ -401,6 +401,28 @@ def test_sr_levels_are_neighbours_and_seed_dependent(orc):
     assert ((q == lo) | (q == hi)).all()
 
 
+@pytest.mark.parametrize("absmax,tiny,q_expected", [
+    (7.0, 2.0 ** -149, 1),      # s = 1: t = 2^-149 > 0 = u
+    (7.0, -2.0 ** -149, 0),     # floor(t) = -1, p = fl(1 - 2^-149) = 1 > u
+    (7.0, 0.0, 0),
+    (7.0, -0.0, 0),
+    (10.5, 2.0 ** -149, 1),     # s = 1.5: 2^-149 / 1.5 rounds up to 2^-149
+    (14.0, 2.0 ** -149, 0),     # s = 2: exactly 2^-150, a tie, rounds to even 0
+    (21.0, 2.0 ** -149, 0),     # s = 3: a third of the smallest subnormal rounds to 0
+])
+def test_sr_tiny_quotient_where_u_is_zero(orc, absmax, tiny, q_expected):
+    # u = 0 exactly where the low 23 bits of the element's Philox word are 0;
+    # there stochastic rounding sends t to floor(t) + 1 iff t - floor(t) > 0,
+    # so the sign and zeroness of the correctly rounded quotient decide q.
+    words = orc.random_words(11, 0, 0, 1 << 24)
+    h = int(np.nonzero((words & 0x7FFFFF) == 0)[0][0])
+    x = np.array([absmax, tiny, 0, 0, 0, 0, 0, 0], np.float32)
+    codes, scales = orc.quantize_pack(x, orc.params(4, 8, orc.SR, seed=11, index_offset=h - 1))
+    assert scales[0] == np.float16(absmax / 7).view(np.uint16)
+    q = codes_to_q(unpack_codes(codes, 4, 8), 4)
+    assert q[0] == 7 and q[1] == q_expected
+
+
 @pytest.mark.parametrize("bits,rounding", [(2, 1), (4, 0), (8, 1), (1, 0)])
 def test_error_feedback_telescopes(orc, bits, rounding):
     # Over T steps with error feedback, sum_t s_t*q_t = sum_t g_t - e_T + (the
