@@ -70,6 +70,86 @@ __device__ __forceinline__ void load_row_codes(const DecArgs& a, int64_t row, Ro
     }
 }
 
+// The rest of a row once its rank sum is in registers: the optional fp32 sum,
+// then stage-2 error feedback, block statistic, requantisation, packing and
+// the new stage-2 error.  `e2` holds the row's incoming stage-2 error (read
+// only when a.err2 is set); `red` is this row's half of the team exchange.
+template <int BOUT, bool SR>
+__device__ __forceinline__ void finish_row(const DecArgs& a, int64_t e0, int valid, const float (&acc)[8],
+                                           const float (&e2)[8], float* red)
+{
+    const int64_t n = a.n;
+    const int64_t piece = e0 >> 3;
+    if (a.sum_out != nullptr) {
+        if (valid == 8) {
+            st8_f32(a.sum_out + e0, acc);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) if (j < valid) a.sum_out[e0 + j] = acc[j];
+        }
+    }
+
+    if constexpr (BOUT != 0) {
+        const Team team = make_team(a.log2Bout);
+        float v[8];
+        if (valid == 8) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = a.err2 != nullptr ? __fadd_rn(acc[j], e2[j]) : acc[j];
+        } else if (a.err2 != nullptr) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = (j < valid) ? __fadd_rn(acc[j], e2[j]) : 0.0f;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = (j < valid) ? acc[j] : 0.0f;
+        }
+
+        float stat;
+        if constexpr (BOUT == 1) {
+            stat = __fadd_rn(__fadd_rn(__fadd_rn(fabsf(v[0]), fabsf(v[1])), __fadd_rn(fabsf(v[2]), fabsf(v[3]))),
+                             __fadd_rn(__fadd_rn(fabsf(v[4]), fabsf(v[5])), __fadd_rn(fabsf(v[6]), fabsf(v[7]))));
+        } else {
+            stat = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                         fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+        }
+        stat = team_reduce<BOUT == 1>(stat, team, red);
+
+        const int64_t blk = e0 >> a.log2Bout;
+        int n_valid = 1 << a.log2Bout;
+        if constexpr (BOUT == 1) {
+            const int64_t left = n - (blk << a.log2Bout);
+            if (left < n_valid) n_valid = left > 0 ? (int)left : 1;
+        }
+        const __half sh = block_scale<BOUT>(stat, n_valid);
+        const float s2 = __half2float(sh);
+
+        uint32_t rw[8];
+        if constexpr (SR && BOUT > 1) {
+            random_words8(a.index_offset + (uint64_t)e0, a.keys, (uint32_t)(a.index_offset & 3u), rw);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) rw[j] = 0u;
+        }
+        Packed<BOUT> c;
+        float q[8];
+        quantize8<BOUT, (SR && BOUT > 1)>(v, s2, scale_reciprocal(s2), rw, c, q);
+
+        if (e0 < (a.nb_out << a.log2Bout)) store_codes<BOUT>(a.codes_out, piece, c);
+        if (team.lane == 0 && blk < a.nb_out) a.scales_out[blk] = __half_as_ushort(sh);
+
+        if (a.err2 != nullptr) {
+            float e[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) e[j] = feedback<BOUT>(v[j], s2, q[j]);
+            if (valid == 8) {
+                st8_f32(a.err2 + e0, e);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) if (j < valid) a.err2[e0 + j] = e[j];
+            }
+        }
+    }
+}
+
 // BOUT == 0: no requantisation (sum only).  MANY: W may exceed 8 (ranks 8..W-1
 // are taken in groups of 8 inside the row; the kernel gets a larger register
 // budget).  The row loop is software-pipelined: the next row's codes and
@@ -140,74 +220,7 @@ decode_kernel(const DecArgs a)
         // prefetch: the next row's codes overlap this row's requantisation
         if (row + gridDim.x < rows) load_row_codes<BIN, KW>(a, row + gridDim.x, cur);
 
-        if (a.sum_out != nullptr) {
-            if (valid == 8) {
-                st8_f32(a.sum_out + e0, acc);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) if (j < valid) a.sum_out[e0 + j] = acc[j];
-            }
-        }
-
-        if constexpr (BOUT != 0) {
-            const Team team = make_team(a.log2Bout);
-            float v[8];
-            if (valid == 8) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[j] = a.err2 != nullptr ? __fadd_rn(acc[j], e2[j]) : acc[j];
-            } else if (a.err2 != nullptr) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[j] = (j < valid) ? __fadd_rn(acc[j], e2[j]) : 0.0f;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[j] = (j < valid) ? acc[j] : 0.0f;
-            }
-
-            float stat;
-            if constexpr (BOUT == 1) {
-                stat = __fadd_rn(__fadd_rn(__fadd_rn(fabsf(v[0]), fabsf(v[1])), __fadd_rn(fabsf(v[2]), fabsf(v[3]))),
-                                 __fadd_rn(__fadd_rn(fabsf(v[4]), fabsf(v[5])), __fadd_rn(fabsf(v[6]), fabsf(v[7]))));
-            } else {
-                stat = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
-                             fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
-            }
-            stat = team_reduce<BOUT == 1>(stat, team, red[parity]);
-
-            const int64_t blk = e0 >> a.log2Bout;
-            int n_valid = 1 << a.log2Bout;
-            if constexpr (BOUT == 1) {
-                const int64_t left = n - (blk << a.log2Bout);
-                if (left < n_valid) n_valid = left > 0 ? (int)left : 1;
-            }
-            const __half sh = block_scale<BOUT>(stat, n_valid);
-            const float s2 = __half2float(sh);
-
-            uint32_t rw[8];
-            if constexpr (SR && BOUT > 1) {
-                random_words8(a.index_offset + (uint64_t)e0, a.keys, (uint32_t)(a.index_offset & 3u), rw);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) rw[j] = 0u;
-            }
-            Packed<BOUT> c;
-            float q[8];
-            quantize8<BOUT, (SR && BOUT > 1)>(v, s2, scale_reciprocal(s2), rw, c, q);
-
-            if (e0 < (a.nb_out << a.log2Bout)) store_codes<BOUT>(a.codes_out, piece, c);
-            if (team.lane == 0 && blk < a.nb_out) a.scales_out[blk] = __half_as_ushort(sh);
-
-            if (a.err2 != nullptr) {
-                float e[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) e[j] = feedback<BOUT>(v[j], s2, q[j]);
-                if (valid == 8) {
-                    st8_f32(a.err2 + e0, e);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) if (j < valid) a.err2[e0 + j] = e[j];
-                }
-            }
-        }
+        finish_row<BOUT, SR>(a, e0, valid, acc, e2, red[parity]);
     }
 }
 
