@@ -197,9 +197,10 @@ def run_ours(args, rank, world, local_rank):
     n, W = args.n, W_RANKS
 
     # CPU baseline first (the oracle is single threaded, rank 0, N=1 only)
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(torch, synth, args.cpu_sample)
+        cpu_all = cpu_all_cores_sample(args.cpu_sample)
 
     ar = AllReduceW8(torch, bc, synth, n, W, dev)
     stream = torch.cuda.current_stream()
@@ -290,6 +291,7 @@ def run_ours(args, rank, world, local_rank):
                        "ms_per_step": round(e2e["step_ms"], 3)}
     if cpu:
         line["cpu_baseline"] = cpu
+        line["cpu_baseline_all_cores"] = cpu_all
     print(json.dumps(line), flush=True)
 
 
@@ -385,6 +387,25 @@ def _sample_inputs(S):
     return xs
 
 
+def _oracle_sample_threads(O, xs_bits, S, threads):
+    """The same sampled step split into `threads` block-aligned slices, each an
+    independent problem (zero error buffers, its own slice of every rank), run
+    on host threads; the oracle's C functions release the GIL."""
+    import concurrent.futures as cf
+    unit = BLOCK * 64
+    per = -(-S // (threads * unit)) * unit
+    bounds = [(lo, min(lo + per, S)) for lo in range(0, S, per)]
+
+    def one(b):
+        lo, hi = b
+        _oracle_sample_step(O, [x[lo:hi] for x in xs_bits], hi - lo)
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, bounds))
+    return time.perf_counter() - t0, len(bounds)
+
+
 def cpu_baseline_sample(torch, synth, S):
     import oracle as O
     O.build()
@@ -393,6 +414,17 @@ def cpu_baseline_sample(torch, synth, S):
     return {"value": round(W_RANKS * S * 4 / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"8 rank encoders over {S} bf16 elements each + the W=8 decoder over "
                       f"{S} elements (one chunk), single-threaded C++ oracle, {t:.2f} s"}
+
+
+def cpu_all_cores_sample(S):
+    """A second CPU figure: the unchanged oracle on every host core at once."""
+    import oracle as O
+    xs = _sample_inputs(S)
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    t, used = _oracle_sample_threads(O, xs, S, threads)
+    return {"value": round(W_RANKS * S * 4 / t / 1e9, 4), "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"the cpu_baseline sample split into {used} block-aligned slices on {used} host "
+                      f"threads, {t:.2f} s"}
 
 
 def run_reference(args, rank, world):
