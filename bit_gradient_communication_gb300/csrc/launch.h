@@ -18,12 +18,12 @@ constexpr uint32_t kPhiloxW0 = 0x9E3779B9u, kPhiloxW1 = 0xBB67AE85u;
 // take every round key from the parameter bank.  Round r uses the key
 // (k0 + r W0, k1 + r W1) mod 2^32.  Counter words 2 and 3 are the same for
 // every element of a launch (the Philox stream and 0), so the second product
-// of round 0 is a launch constant too and is folded into the two x-terms it
-// feeds: x0 = hi(M1 stream) ^ k0 (round 0) and x1 = lo(M1 stream) ^ (k0 + W0)
-// (round 1).
+// of the first Philox round is a launch constant too and is folded into the
+// two x-terms it feeds: x0 = hi(M1 stream) ^ k0 (first Philox round) and
+// x1 = lo(M1 stream) ^ (k0 + W0) (second Philox round).
 struct PhiloxKeys {
     uint32_t x0, x1;
-    uint32_t k0[10];        // k0 + r W0; rounds 2..9 read it
+    uint32_t k0[10];        // k0 + r W0; Philox rounds r = 2..9 read it
     uint32_t k1[10];        // k1 + r W1
 };
 
