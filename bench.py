@@ -464,6 +464,13 @@ def _timed(torch, fn, K, flush=None):
     """Average device time of fn() over K calls (events on the current stream);
     flush() runs between calls, outside the timed intervals."""
     st = torch.cuda.current_stream()
+    if flush is not None:
+        # one untimed round first: the flush's own kernels load and allocate on
+        # first use, and a host stall there would drain the queue into the
+        # first timed interval
+        flush()
+        fn()
+        torch.cuda.synchronize()
     total = 0.0
     for _ in range(K):
         if flush is not None:
