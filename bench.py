@@ -298,9 +298,12 @@ def run_ours(args, rank, world, local_rank):
 def run_e2e(torch, bc, ar, args, dev):
     """Host -> device copies of the 8 ranks' gradients (pinned), the step, and
     the requantised codes + scales back to the host, all inside the timed
-    region.  Rank w's copy runs on a copy stream and overlaps rank w-1's
-    encoder; chunk c's result goes back on a second copy stream as soon as
-    chunk c's decoder has finished."""
+    region.  Copies run on their own streams and wait only for what they
+    overwrite: rank w's gradient copy for the previous step's encoder w, chunk
+    c's decoder for the previous step's copy-out of chunk c.  So the next
+    step's copies in stream behind this step's kernels, as in a training loop
+    that overlaps communication with compute, while every step still moves
+    its own bytes across the host link."""
     W, n = ar.W, ar.n
     host_x = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(W)]
     for w in range(W):
@@ -313,21 +316,28 @@ def run_e2e(torch, bc, ar, args, dev):
     h2d = sum(t.numel() * t.element_size() for t in host_x)
     d2h = host_codes.numel() + host_scales.numel() * 2
     b2, B2 = ar.p2.bits, ar.p2.block
+    enc_done = [None] * W                      # previous step's encoder w has read x[w]
+    out_done = [None] * len(ar.chunks)         # previous step's chunk c is back on the host
 
     def step():
-        h2d_stream.wait_stream(compute)         # the previous step has consumed x
-        done = []
+        arrived = []
         for w in range(W):
             with torch.cuda.stream(h2d_stream):
+                if enc_done[w] is not None:
+                    h2d_stream.wait_event(enc_done[w])
                 ar.x[w].copy_(host_x[w], non_blocking=True)
                 e = torch.cuda.Event()
                 e.record(h2d_stream)
-            done.append(e)
+            arrived.append(e)
         for w in range(W):
-            compute.wait_event(done[w])
+            compute.wait_event(arrived[w])
             ar.encode_rank(w)
-        d2h_stream.wait_stream(compute)
+            e = torch.cuda.Event()
+            e.record(compute)
+            enc_done[w] = e
         for c, (lo, hi) in enumerate(ar.chunks):
+            if out_done[c] is not None:
+                compute.wait_event(out_done[c])
             ar.decode_chunk(c)
             ev = torch.cuda.Event()
             ev.record(compute)
@@ -337,7 +347,9 @@ def run_e2e(torch, bc, ar, args, dev):
                 host_codes[lo * b2 // 8: hi2 * b2 // 8].copy_(ar.codes_out[lo * b2 // 8: hi2 * b2 // 8],
                                                               non_blocking=True)
                 host_scales[lo // B2: hi2 // B2].copy_(ar.scales_out[lo // B2: hi2 // B2], non_blocking=True)
-        compute.wait_stream(d2h_stream)
+                e = torch.cuda.Event()
+                e.record(d2h_stream)
+            out_done[c] = e
 
     steps = max(1, min(args.steps, args.e2e_steps))
     for _ in range(2):
@@ -346,10 +358,17 @@ def run_e2e(torch, bc, ar, args, dev):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(compute)
+    h2d_stream.wait_event(t0)                  # no copy of the timed steps starts before t0
+    d2h_stream.wait_event(t0)
     for _ in range(steps):
         step()
+    compute.wait_stream(d2h_stream)            # the last step's results are on the host
+    compute.wait_stream(h2d_stream)
     t1.record(compute)
     torch.cuda.synchronize()
+    # the copies back must hold the last step's result (no copy raced its decoder)
+    if not (torch.equal(host_codes, ar.codes_out.cpu()) and torch.equal(host_scales, ar.scales_out.cpu())):
+        raise RuntimeError("e2e: host copy of the result differs from the device result")
     return {"step_ms": t0.elapsed_time(t1) / steps, "h2d": h2d, "d2h": d2h}
 
 
