@@ -5,6 +5,7 @@
 #include "bitscom.h"
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <chrono>
 #include <cstdint>
@@ -25,6 +26,16 @@ struct bitscom_sched {
 namespace {
 
 constexpr int kMaxStreams = 8;
+
+// NVTX range over a scope of host-side issue (header-only NVTX3: nearly free
+// unless a profiler is attached), so a trace shows which bucket and phase
+// issued which launches.
+struct Range {
+    explicit Range(const char* name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range&) = delete;
+    Range& operator=(const Range&) = delete;
+};
 
 int64_t plan_unit(int32_t block) { return block > 128 ? block : 128; }
 
@@ -136,8 +147,10 @@ bitscom_status bitscom_sched_quantize_pack(bitscom_sched* s, const void* x, bits
     const int64_t count = per == 0 ? 1 : (n + per - 1) / per;
     const int used = count < s->n_streams ? (int)count : s->n_streams;
     cudaStream_t caller = static_cast<cudaStream_t>(cuda_stream);
+    Range whole("bitscom.sched.quantize_pack");
     st = fork(s, caller, used);
     for (int64_t k = 0; st == BITSCOM_OK && k < count; ++k) {
+        Range bucket("bitscom.bucket");
         const int64_t b0 = per == 0 ? 0 : k * per;
         const int64_t nb = per == 0 ? n : (n - b0 < per ? n - b0 : per);
         bitscom_qparams q = *p;
@@ -185,6 +198,7 @@ bitscom_status bitscom_sched_allreduce(bitscom_sched* s, int32_t W, const void* 
     const int64_t count = per == 0 ? 1 : (n + per - 1) / per;
     const int used = count < s->n_streams ? (int)count : s->n_streams;
     cudaStream_t caller = static_cast<cudaStream_t>(cuda_stream);
+    Range whole("bitscom.sched.allreduce");
     bitscom_status st = fork(s, caller, used);
     std::vector<const void*> cin(W);
     std::vector<const uint16_t*> sin(W);
@@ -193,15 +207,19 @@ bitscom_status bitscom_sched_allreduce(bitscom_sched* s, int32_t W, const void* 
         const int64_t b0 = per == 0 ? 0 : k * per;
         const int64_t nbk = per == 0 ? n : (n - b0 < per ? n - b0 : per);
         // stage 1 on every rank
-        for (int w = 0; st == BITSCOM_OK && w < W; ++w) {
-            bitscom_qparams q = p1[w];
-            q.index_offset = p1[w].index_offset + (uint64_t)b0;
-            st = bitscom_quantize_pack(static_cast<const char*>(x[w]) + b0 * esz, dt, nbk,
-                                       (err && err[w]) ? err[w] + b0 : nullptr, &q,
-                                       static_cast<char*>(codes[w]) + offset_bytes(b0, p1[w].bits),
-                                       scales[w] + b0 / B1, str);
+        {
+            Range enc("bitscom.bucket.encode");
+            for (int w = 0; st == BITSCOM_OK && w < W; ++w) {
+                bitscom_qparams q = p1[w];
+                q.index_offset = p1[w].index_offset + (uint64_t)b0;
+                st = bitscom_quantize_pack(static_cast<const char*>(x[w]) + b0 * esz, dt, nbk,
+                                           (err && err[w]) ? err[w] + b0 : nullptr, &q,
+                                           static_cast<char*>(codes[w]) + offset_bytes(b0, p1[w].bits),
+                                           scales[w] + b0 / B1, str);
+            }
         }
         // all-to-all by pointer arithmetic: chunk c = units [c*cu, (c+1)*cu)
+        Range dec("bitscom.bucket.decode");
         const int64_t units = (nbk + U - 1) / U;
         const int64_t cu = (units + W - 1) / W;
         for (int c = 0; st == BITSCOM_OK && c < W; ++c) {
