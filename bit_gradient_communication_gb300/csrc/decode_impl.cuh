@@ -224,9 +224,186 @@ decode_kernel(const DecArgs a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Eight ranks of 4-bit codes requantised to 4 bits (the W = 8 all-reduce of one
+// eight-GPU node) with 16 elements per thread: 256-thread CTAs over the same
+// 4096-element rows, each rank's codes of a thread one 8-byte load and one
+// scale (blocks of >= 16), and the block statistic, scale, reciprocal and
+// loop bookkeeping paid once per 16 elements instead of per 8.  The
+// arithmetic per element is that of decode_kernel, so the results are the
+// same bits.  Needs 8-byte aligned code pointers and blocks of >= 16 on both
+// sides; otherwise decode_kernel runs.
+// ---------------------------------------------------------------------------
+constexpr int kThreads16 = 256;
+
+__device__ __forceinline__ Team make_team16(int log2B)
+{
+    Team t;
+    t.size = 1 << (log2B - 4);
+    t.lane = threadIdx.x & (t.size - 1);
+    t.id = threadIdx.x >> (log2B - 4);
+    t.warps = t.size >> 5;
+    return t;
+}
+
+template <bool SR>
+__global__ void __launch_bounds__(kThreads16, 3) decode16_w8_kernel(const DecArgs a)
+{
+    __shared__ float red[2][kThreads16 / 32];
+    const int64_t n = a.n;
+    const int rows = (int)((n + kRow - 1) / kRow);       // < 2^31 (decode16_fits)
+    const int tid = threadIdx.x;
+    const Team team = make_team16(a.log2Bout);
+
+    uint2 cc[8];
+    uint32_t sc[4];                                  // the 8 ranks' fp16 scales, two per word
+    auto load = [&](int row) {
+        const int64_t e0 = (int64_t)row * kRow + tid * 16;
+        if (e0 >= n) return;
+        const int64_t off = e0 >> 1;                 // 4-bit codes: 8 bytes per 16 elements
+        const int64_t blk = e0 >> a.log2Bin;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) cc[k] = __ldg(reinterpret_cast<const uint2*>(a.codes[k] + off));
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            sc[k] = __byte_perm(__ldg(a.scales[2 * k] + blk), __ldg(a.scales[2 * k + 1] + blk), 0x5410);
+    };
+    if ((int)blockIdx.x < rows) load(blockIdx.x);
+    int parity = 0;
+    for (int row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
+        const int64_t e0 = (int64_t)row * kRow + tid * 16;
+        const int64_t rem = n - e0;
+        const int valid = rem <= 0 ? 0 : (rem >= 16 ? 16 : (int)rem);
+
+        float e2[16];
+        if (a.err2 != nullptr) {
+            if (valid == 16) {
+                float lo[8], hi[8];
+                ld8_f32(a.err2 + e0, lo);
+                ld8_f32(a.err2 + e0 + 8, hi);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) { e2[j] = lo[j]; e2[j + 8] = hi[j]; }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) e2[j] = (j < valid) ? a.err2[e0 + j] : 0.0f;
+            }
+        }
+
+        float lo[8], hi[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { lo[j] = 0.0f; hi[j] = 0.0f; }
+        if (valid > 0) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                Packed<4> c0, c1;
+                c0.w[0] = cc[k].x;
+                c1.w[0] = cc[k].y;
+                const unsigned short sk = (unsigned short)((k & 1) ? sc[k >> 1] >> 16 : sc[k >> 1] & 0xFFFFu);
+                accumulate_rank<4>(c0, sk, k == 0, lo);
+                accumulate_rank<4>(c1, sk, k == 0, hi);
+            }
+        }
+        if (row + (int)gridDim.x < rows) load(row + gridDim.x);   // overlaps the requantisation
+
+        if (a.sum_out != nullptr) {
+            if (valid == 16) {
+                st8_f32(a.sum_out + e0, lo);
+                st8_f32(a.sum_out + e0 + 8, hi);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (j < valid) a.sum_out[e0 + j] = j < 8 ? lo[j] : hi[j - 8];
+            }
+        }
+
+        // stage-2 error feedback, block statistic over 16 elements, requantise
+        float v0[8], v1[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float x0 = lo[j], x1 = hi[j];
+            if (a.err2 != nullptr) { x0 = __fadd_rn(x0, e2[j]); x1 = __fadd_rn(x1, e2[j + 8]); }
+            v0[j] = j < valid ? x0 : 0.0f;
+            v1[j] = j + 8 < valid ? x1 : 0.0f;
+        }
+        float stat = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) stat = fmaxf(stat, fmaxf(fabsf(v0[j]), fabsf(v1[j])));
+        stat = team_reduce<false>(stat, team, red[parity]);
+        const int64_t blk = e0 >> a.log2Bout;
+        const __half sh = block_scale<4>(stat, 1 << a.log2Bout);
+        const float s2 = __half2float(sh);
+        const float y2 = scale_reciprocal(s2);
+
+        uint32_t rw0[8], rw1[8];
+        if constexpr (SR) {
+            const uint32_t shift = (uint32_t)(a.index_offset & 3u);
+            random_words8(a.index_offset + (uint64_t)e0, a.keys, shift, rw0);
+            random_words8(a.index_offset + (uint64_t)e0 + 8, a.keys, shift, rw1);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) { rw0[j] = 0u; rw1[j] = 0u; }
+        }
+        Packed<4> c0, c1;
+        float q0[8], q1[8];
+        quantize8<4, SR>(v0, s2, y2, rw0, c0, q0);
+        quantize8<4, SR>(v1, s2, y2, rw1, c1, q1);
+        if (e0 < (a.nb_out << a.log2Bout))
+            *reinterpret_cast<uint2*>(a.codes_out + (e0 >> 1)) = make_uint2(c0.w[0], c1.w[0]);
+        if (team.lane == 0 && blk < a.nb_out) a.scales_out[blk] = __half_as_ushort(sh);
+
+        if (a.err2 != nullptr) {
+            float f0[8], f1[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                f0[j] = feedback<4>(v0[j], s2, q0[j]);
+                f1[j] = feedback<4>(v1[j], s2, q1[j]);
+            }
+            if (valid == 16) {
+                st8_f32(a.err2 + e0, f0);
+                st8_f32(a.err2 + e0 + 8, f1);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (j < valid) a.err2[e0 + j] = j < 8 ? f0[j] : f1[j - 8];
+            }
+        }
+    }
+}
+
+template <bool SR>
+static cudaError_t run_decode16_w8(const DecArgs& a, cudaStream_t st)
+{
+    static std::atomic<int> cap{0};
+    const int64_t rows = (a.n + kRow - 1) / kRow;
+    int c = cap.load(std::memory_order_relaxed);
+    if (c == 0) {
+        int dev = 0, occ = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode16_w8_kernel<SR>, kThreads16, 0);
+        c = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
+        cap.store(c, std::memory_order_relaxed);
+    }
+    const int grid = (int)(rows < c ? rows : c);
+    decode16_w8_kernel<SR><<<grid, kThreads16, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+static bool decode16_fits(const DecArgs& a)
+{
+    if (a.W != 8 || a.log2Bin < 4 || a.log2Bout < 4 || a.codes_out == nullptr || a.n >= ((int64_t)1 << 42))
+        return false;
+    for (int k = 0; k < 8; ++k)
+        if ((reinterpret_cast<uintptr_t>(a.codes[k]) & 7u) != 0) return false;
+    return (reinterpret_cast<uintptr_t>(a.codes_out) & 7u) == 0;
+}
+
 template <int BIN, int BOUT, bool SR, bool MANY, int KW>
 static cudaError_t run_decode_kw(const DecArgs& a, cudaStream_t st)
 {
+    if constexpr (KW == 8 && BIN == 4 && BOUT == 4 && !MANY) {
+        if (decode16_fits(a)) return run_decode16_w8<SR>(a, st);
+    }
     static std::atomic<int> cap{0};
     const int64_t rows = (a.n + kRow - 1) / kRow;
     const int grid = grid_size(decode_kernel<BIN, BOUT, SR, MANY, KW>, cap, rows);
