@@ -207,6 +207,48 @@ def test_decoder_matches_oracle(bin_, bout, Bin, Bout, W, mode):
             assert np.array_equal(e2_g.host(np.uint32), e2_ref.view(np.uint32)), f"e2' differs n={n}"
 
 
+@pytest.mark.parametrize("offset", [0, 4])
+@pytest.mark.parametrize("sr", [False, True])
+def test_decoder_w8_alignment_paths(offset, sr):
+    # Eight ranks of 4-bit codes take a 16-elements-per-thread decoder when the
+    # code pointers are 8-byte aligned (offset 0) and the general one when they
+    # are only 4-byte aligned (offset 4); both must give the oracle's bits, with
+    # and without the fp32 sum output.
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(31 + offset + sr)
+    W, B = 8, 128
+    for n in (4096 * 3 + 77, 16 * 40):
+        for with_sum in (False, True):
+            ins = [_random_codes(rng, n, 4, B) for _ in range(W)]
+            nb = bc.packed_bytes(n, 4, B)
+            cin = []
+            for c, _ in ins:
+                buf = torch.zeros(nb + 16, dtype=torch.uint8, device="cuda")
+                buf[offset:offset + nb].copy_(torch.from_numpy(c).cuda())
+                cin.append(buf[offset:offset + nb])
+            sin = [torch.from_numpy(sc.view(np.int16)).cuda() for _, sc in ins]
+            e2 = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+            e2_g = torch.from_numpy(e2.copy()).cuda()
+            cob = torch.zeros(nb + 16, dtype=torch.uint8, device="cuda")
+            co = cob[offset:offset + nb]
+            so = torch.zeros(bc.num_blocks(n, B), dtype=torch.int16, device="cuda")
+            pout = bc.QParams(4, B, bc.SR if sr else bc.RTN, seed=5, index_offset=12, philox_stream=1)
+            sm, _, _ = bc.unpack_dequant_reduce_requant(cin, sin, n, bc.QParams(4, B),
+                                                        sum_out=True if with_sum else None, err2=e2_g,
+                                                        p_out=pout, codes_out=co, scales_out=so)
+            torch.cuda.synchronize()
+            e2_ref = e2.copy()
+            s_ref, c_ref, sc_ref = O.unpack_dequant_reduce_requant(
+                [c for c, _ in ins], [sc for _, sc in ins], n, O.params(4, B), True, e2_ref,
+                O.params(4, B, O.SR if sr else O.RTN, seed=5, index_offset=12, philox_stream=1))
+            tag = f"n={n} sum={with_sum}"
+            assert co.cpu().numpy().tobytes() == c_ref.tobytes(), tag
+            assert np.array_equal(so.cpu().numpy().view(np.uint16), sc_ref), tag
+            assert np.array_equal(e2_g.cpu().numpy().view(np.uint32), e2_ref.view(np.uint32)), tag
+            if with_sum:
+                assert np.array_equal(sm.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), tag
+
+
 def test_decoder_requant_without_sum_output():
     torch, bc = need_gpu()
     rng = np.random.default_rng(11)
