@@ -234,17 +234,6 @@ decode_kernel(const DecArgs a)
 // same bits.  Needs 8-byte aligned code pointers and blocks of >= 16 on both
 // sides; otherwise decode_kernel runs.
 // ---------------------------------------------------------------------------
-constexpr int kThreads16 = 256;
-
-__device__ __forceinline__ Team make_team16(int log2B)
-{
-    Team t;
-    t.size = 1 << (log2B - 4);
-    t.lane = threadIdx.x & (t.size - 1);
-    t.id = threadIdx.x >> (log2B - 4);
-    t.warps = t.size >> 5;
-    return t;
-}
 
 template <bool SR>
 __global__ void __launch_bounds__(kThreads16, 3) decode16_w8_kernel(const DecArgs a)

@@ -81,6 +81,30 @@ def test_encoder_is_deterministic():
     assert a[0].tobytes() == b[0].tobytes() and np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
 
 
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_encoder_sr_alignment_paths(bits, dt):
+    # Stochastic rounding without error feedback takes a 16-elements-per-thread
+    # encoder when the code pointer is aligned to 2b bytes and the general one
+    # when it is aligned to b bytes only; both must give the oracle's bits.
+    torch, bc = need_gpu()
+    n = 3 * 4096 + 77
+    x, _ = _inputs(n, dt, 123 + bits)
+    xh = x if dt == "f32" else bf16_bits_of(torch, x)
+    xg = torch.from_numpy(xh).cuda() if dt == "f32" else torch.from_numpy(xh.view(np.int16)).cuda().view(torch.bfloat16)
+    p = bc.QParams(bits, 128, bc.SR, seed=17, index_offset=6)
+    c_ref, s_ref = O.quantize_pack(xh, O.params(bits, 128, O.SR, seed=17, index_offset=6))
+    nb = bc.packed_bytes(n, bits, 128)
+    for offset in (0, bits):
+        buf = torch.zeros(nb + 32, dtype=torch.uint8, device="cuda")
+        codes = buf[offset:offset + nb]
+        scales = torch.zeros(bc.num_blocks(n, 128), dtype=torch.int16, device="cuda")
+        bc.quantize_pack(xg, p, None, codes, scales)
+        torch.cuda.synchronize()
+        assert codes.cpu().numpy().tobytes() == c_ref.tobytes(), f"offset {offset}"
+        assert np.array_equal(scales.cpu().numpy().view(np.uint16), s_ref), f"offset {offset}"
+
+
 def test_encoder_special_blocks():
     # zero blocks, underflowing and subnormal scales, saturation, negative zero
     torch, bc = need_gpu()
