@@ -155,13 +155,13 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// Stochastic rounding with 16 elements per thread (2-, 4- and 8-bit codes,
-// blocks of >= 16, no rotation; used without error feedback, see
-// run_encode): three 256-thread CTAs per SM over the same
-// 4096-element rows.  These encoders are bound by instruction issue (two
-// Philox4x32-10 calls per 8 elements), so the per-row work -- block statistic
-// exchange, scale, reciprocal, index and loop bookkeeping -- is paid once per
-// 16 elements.  The per-element arithmetic is that of encode_kernel, so the
+// 16 elements per thread (2-, 4- and 8-bit codes, blocks of >= 16, no
+// rotation; used without error feedback, see run_encode): three 256-thread
+// CTAs per SM over the same 4096-element rows.  Without the error buffer an
+// encoder moves only ~4.3-5 bytes per element, so instruction issue binds
+// (stochastic rounding adds two Philox4x32-10 calls per 8 elements); the
+// per-row work -- block statistic exchange, scale, reciprocal, index and loop
+// bookkeeping -- is paid once per 16 elements.  The per-element arithmetic is that of encode_kernel, so the
 // results are the same bits.  Needs code pointers aligned to the 16 codes'
 // 2b bytes; otherwise encode_kernel runs.
 // ---------------------------------------------------------------------------
@@ -216,8 +216,8 @@ __device__ __forceinline__ void load_row16(const EncArgs& a, int row, RowIn16<IN
     }
 }
 
-template <int IN, int BITS, bool EF>
-__global__ void __launch_bounds__(kThreads16, 3) encode16_sr_kernel(const EncArgs a)
+template <int IN, int BITS, bool EF, bool SR>
+__global__ void __launch_bounds__(kThreads16, 3) encode16_kernel(const EncArgs a)
 {
     __shared__ float red[2][kThreads16 / 32];
     const Team team = make_team16(a.log2B);
@@ -255,12 +255,17 @@ __global__ void __launch_bounds__(kThreads16, 3) encode16_sr_kernel(const EncArg
         const float y = scale_reciprocal(s);
 
         uint32_t rw0[8], rw1[8];
-        random_words8(a.index_offset + (uint64_t)e0, a.keys, shift, rw0);
-        random_words8(a.index_offset + (uint64_t)e0 + 8, a.keys, shift, rw1);
+        if constexpr (SR) {
+            random_words8(a.index_offset + (uint64_t)e0, a.keys, shift, rw0);
+            random_words8(a.index_offset + (uint64_t)e0 + 8, a.keys, shift, rw1);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) { rw0[j] = 0u; rw1[j] = 0u; }
+        }
         Packed<BITS> c0, c1;
         float q0[8], q1[8];
-        quantize8<BITS, true>(v0, s, y, rw0, c0, q0);
-        quantize8<BITS, true>(v1, s, y, rw1, c1, q1);
+        quantize8<BITS, SR>(v0, s, y, rw0, c0, q0);
+        quantize8<BITS, SR>(v1, s, y, rw1, c1, q1);
         if (e0 < (a.nb << a.log2B)) {
             uint8_t* p = a.codes + e0 * BITS / 8;
             if constexpr (BITS == 2) {
@@ -292,8 +297,8 @@ __global__ void __launch_bounds__(kThreads16, 3) encode16_sr_kernel(const EncArg
     }
 }
 
-template <int IN, int BITS, bool EF>
-static cudaError_t run_encode16_sr(const EncArgs& a, cudaStream_t st)
+template <int IN, int BITS, bool EF, bool SR>
+static cudaError_t run_encode16(const EncArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};
     const int64_t rows = (a.n + kRow - 1) / kRow;
@@ -302,12 +307,12 @@ static cudaError_t run_encode16_sr(const EncArgs& a, cudaStream_t st)
         int dev = 0, occ = 0, sms = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode16_sr_kernel<IN, BITS, EF>, kThreads16, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode16_kernel<IN, BITS, EF, SR>, kThreads16, 0);
         c = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
         cap.store(c, std::memory_order_relaxed);
     }
     const int grid = (int)(rows < c ? rows : c);
-    encode16_sr_kernel<IN, BITS, EF><<<grid, kThreads16, 0, st>>>(a);
+    encode16_kernel<IN, BITS, EF, SR><<<grid, kThreads16, 0, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -333,8 +338,8 @@ static cudaError_t run_encode(const EncArgs& a, cudaStream_t st)
 {
     // without error feedback only: with it, the 16-element layout spills and
     // measured slower on the 25 MiB fp32 buckets (0.59-0.64 vs 0.65-0.70)
-    if constexpr (SR && !EF && (BITS == 2 || BITS == 4 || BITS == 8)) {
-        if (encode16_fits(a, BITS)) return run_encode16_sr<IN, BITS, EF>(a, st);
+    if constexpr (!EF && (BITS == 2 || BITS == 4 || BITS == 8)) {
+        if (encode16_fits(a, BITS)) return run_encode16<IN, BITS, EF, SR>(a, st);
     }
     if (a.hadamard == 0) return run_encode_h<IN, BITS, EF, SR, false>(a, st);
     if constexpr (BITS == 2 || BITS == 4 || BITS == 8) {
