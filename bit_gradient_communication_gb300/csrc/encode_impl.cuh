@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// 16 elements per thread (2-, 4- and 8-bit codes, blocks of >= 16, no
+// 16 elements per thread (2-, 4-, 8- and 16-bit codes, blocks of >= 16, no
 // rotation; used without error feedback, see run_encode): three 256-thread
 // CTAs per SM over the same 4096-element rows.  Without the error buffer an
 // encoder moves only ~4.3-5 bytes per element, so instruction issue binds
@@ -272,8 +272,12 @@ __global__ void __launch_bounds__(kThreads16, 3) encode16_kernel(const EncArgs a
                 *reinterpret_cast<uint32_t*>(p) = (c0.w[0] & 0xFFFFu) | (c1.w[0] << 16);
             } else if constexpr (BITS == 4) {
                 *reinterpret_cast<uint2*>(p) = make_uint2(c0.w[0], c1.w[0]);
-            } else {
+            } else if constexpr (BITS == 8) {
                 *reinterpret_cast<uint4*>(p) = make_uint4(c0.w[0], c0.w[1], c1.w[0], c1.w[1]);
+            } else {
+                uint4* q = reinterpret_cast<uint4*>(p);
+                q[0] = make_uint4(c0.w[0], c0.w[1], c0.w[2], c0.w[3]);
+                q[1] = make_uint4(c1.w[0], c1.w[1], c1.w[2], c1.w[3]);
             }
         }
         if (team.lane == 0 && blk < a.nb) a.scales[blk] = __half_as_ushort(sh);
@@ -338,7 +342,7 @@ static cudaError_t run_encode(const EncArgs& a, cudaStream_t st)
 {
     // without error feedback only: with it, the 16-element layout spills and
     // measured slower on the 25 MiB fp32 buckets (0.59-0.64 vs 0.65-0.70)
-    if constexpr (!EF && (BITS == 2 || BITS == 4 || BITS == 8)) {
+    if constexpr (!EF && (BITS == 2 || BITS == 4 || BITS == 8 || BITS == 16)) {
         if (encode16_fits(a, BITS)) return run_encode16<IN, BITS, EF, SR>(a, st);
     }
     if (a.hadamard == 0) return run_encode_h<IN, BITS, EF, SR, false>(a, st);
