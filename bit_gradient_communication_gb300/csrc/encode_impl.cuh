@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// 16 elements per thread (2-, 4-, 8- and 16-bit codes, blocks of >= 16, no
+// 16 elements per thread (1-, 2-, 4-, 8- and 16-bit codes, blocks of >= 16, no
 // rotation; used without error feedback, see run_encode): three 256-thread
 // CTAs per SM over the same 4096-element rows.  Without the error buffer an
 // encoder moves only ~4.3-5 bytes per element, so instruction issue binds
@@ -245,12 +245,29 @@ __global__ void __launch_bounds__(kThreads16, 3) encode16_kernel(const EncArgs a
         }
         if (row + (int)gridDim.x < rows) load_row16<IN, EF>(a, row + gridDim.x, cur);
 
-        float stat = 0.0f;
+        // block statistic: absmax (b >= 2), or for b = 1 the tree sum of |v|
+        // over contiguous halves: this thread's 16 elements are two 8-element
+        // subtrees, and the butterfly over threads joins contiguous halves
+        float stat;
+        if constexpr (BITS == 1) {
+            auto tree8 = [](const float (&v)[8]) {
+                return __fadd_rn(__fadd_rn(__fadd_rn(fabsf(v[0]), fabsf(v[1])), __fadd_rn(fabsf(v[2]), fabsf(v[3]))),
+                                 __fadd_rn(__fadd_rn(fabsf(v[4]), fabsf(v[5])), __fadd_rn(fabsf(v[6]), fabsf(v[7]))));
+            };
+            stat = __fadd_rn(tree8(v0), tree8(v1));
+        } else {
+            stat = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) stat = fmaxf(stat, fmaxf(fabsf(v0[j]), fabsf(v1[j])));
-        stat = team_reduce<false>(stat, team, red[parity]);
+            for (int j = 0; j < 8; ++j) stat = fmaxf(stat, fmaxf(fabsf(v0[j]), fabsf(v1[j])));
+        }
+        stat = team_reduce<BITS == 1>(stat, team, red[parity]);
         const int64_t blk = e0 >> a.log2B;
-        const __half sh = block_scale<BITS>(stat, 1 << a.log2B);
+        int n_valid = 1 << a.log2B;
+        if constexpr (BITS == 1) {
+            const int64_t left = n - (blk << a.log2B);
+            if (left < n_valid) n_valid = left > 0 ? (int)left : 1;
+        }
+        const __half sh = block_scale<BITS>(stat, n_valid);
         const float s = __half2float(sh);
         const float y = scale_reciprocal(s);
 
@@ -268,7 +285,9 @@ __global__ void __launch_bounds__(kThreads16, 3) encode16_kernel(const EncArgs a
         quantize8<BITS, SR>(v1, s, y, rw1, c1, q1);
         if (e0 < (a.nb << a.log2B)) {
             uint8_t* p = a.codes + e0 * BITS / 8;
-            if constexpr (BITS == 2) {
+            if constexpr (BITS == 1) {
+                *reinterpret_cast<uint16_t*>(p) = (uint16_t)((c0.w[0] & 0xFFu) | ((c1.w[0] & 0xFFu) << 8));
+            } else if constexpr (BITS == 2) {
                 *reinterpret_cast<uint32_t*>(p) = (c0.w[0] & 0xFFFFu) | (c1.w[0] << 16);
             } else if constexpr (BITS == 4) {
                 *reinterpret_cast<uint2*>(p) = make_uint2(c0.w[0], c1.w[0]);
@@ -342,7 +361,7 @@ static cudaError_t run_encode(const EncArgs& a, cudaStream_t st)
 {
     // without error feedback only: with it, the 16-element layout spills and
     // measured slower on the 25 MiB fp32 buckets (0.59-0.64 vs 0.65-0.70)
-    if constexpr (!EF && (BITS == 2 || BITS == 4 || BITS == 8 || BITS == 16)) {
+    if constexpr (!EF && BITS != 12) {
         if (encode16_fits(a, BITS)) return run_encode16<IN, BITS, EF, SR>(a, st);
     }
     if (a.hadamard == 0) return run_encode_h<IN, BITS, EF, SR, false>(a, st);
