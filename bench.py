@@ -425,6 +425,29 @@ def _oracle_sample_threads(O, xs_bits, S, threads):
     return time.perf_counter() - t0, len(bounds)
 
 
+def _host_cpu():
+    """The host's CPU model and logical CPU count (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return {"model": model, "logical_cpus": os.cpu_count()}
+
+
 def cpu_baseline_sample(torch, synth, S):
     import oracle as O
     O.build()
@@ -432,7 +455,8 @@ def cpu_baseline_sample(torch, synth, S):
     t = _oracle_sample_step(O, xs, S)
     return {"value": round(W_RANKS * S * 4 / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"8 rank encoders over {S} bf16 elements each + the W=8 decoder over "
-                      f"{S} elements (one chunk), single-threaded C++ oracle, {t:.2f} s"}
+                      f"{S} elements (one chunk), single-threaded C++ oracle, {t:.2f} s",
+            "host": _host_cpu()}
 
 
 def cpu_all_cores_sample(S):
