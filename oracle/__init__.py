@@ -7,7 +7,7 @@ C++ (``bitscom_oracle.cpp``) loaded through ctypes, working on numpy arrays.
 
 Parity status of each function (details in the tests):
   f32_to_f16, f16_to_f32, bf16_to_f32   pinned (exhaustive vs numpy casts)
-  philox4x32_10                          pinned (cuRAND host generator)
+  philox4x32_10, random_word(s)          pinned (cuRAND host generator)
   quantize_pack                          pinned (hand-worked blocks, bounds,
                                          unbiasedness, numpy packbits)
   unpack_dequant_reduce_requant          pinned (W=1 == dequant, hand sums,

@@ -17,6 +17,13 @@
  *
  * All integers are little-endian; codes are produced as a byte stream.
  * Every function returns 0 on success and a nonzero value on a bad argument.
+ *
+ * Parity status: every function here is pinned by tests against values fixed
+ * by the pages and the mathematics (hand-worked blocks, exhaustive format
+ * conversions, cuRAND's host Philox, closed-form bounds, numpy packbits,
+ * scipy's Hadamard matrix), except two readings, which are parity unpinned:
+ * the zero-padded tail block (n mod B != 0) and stochastic rounding at 1 bit
+ * (taken as plain sign).  Nothing outside this code checks those two.
  */
 #ifndef BITSCOM_ORACLE_H
 #define BITSCOM_ORACLE_H
