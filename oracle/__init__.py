@@ -15,7 +15,10 @@ Parity status of each function (details in the tests):
   unpack_dequant, f32_to_bf16            pinned (W=1 decoder sums, torch bf16 cast)
   fwht (Hadamard smoothing)              pinned (scipy Sylvester matrix, involution)
   qwd_encode, qwd_apply                  pinned (hand block, bound, telescoping)
-  tail blocks (n mod B != 0), 1-bit SR   parity unpinned (readings only)
+  tail blocks (n mod B != 0), 1-bit SR   pinned to their readings (hand-worked
+                                         tails, tail == zero-padded block,
+                                         1-bit SR == RTN); the readings
+                                         themselves have no page support
 """
 from __future__ import annotations
 

@@ -21,9 +21,11 @@
  * Parity status: every function here is pinned by tests against values fixed
  * by the pages and the mathematics (hand-worked blocks, exhaustive format
  * conversions, cuRAND's host Philox, closed-form bounds, numpy packbits,
- * scipy's Hadamard matrix), except two readings, which are parity unpinned:
- * the zero-padded tail block (n mod B != 0) and stochastic rounding at 1 bit
- * (taken as plain sign).  Nothing outside this code checks those two.
+ * scipy's Hadamard matrix).  Two readings have no support in the pages: the
+ * zero-padded tail block (n mod B != 0) and stochastic rounding at 1 bit
+ * (taken as plain sign); their implementation is pinned to the reading
+ * (hand-worked tail blocks, tail == zero-padded block, 1-bit SR == RTN), the
+ * reading itself is not.
  */
 #ifndef BITSCOM_ORACLE_H
 #define BITSCOM_ORACLE_H

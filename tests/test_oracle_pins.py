@@ -185,6 +185,46 @@ def test_one_bit_tail_mean_divides_by_valid(orc):
     assert unpack_codes(codes, 1, 8).tolist() == [1, 0, 1, 1, 1, 1, 1, 1]
 
 
+def test_tail_block_hand_worked(orc):
+    # n = 5 in a block of 8 (b = 4): the first five values of the hand-worked
+    # 4-bit block.  The tail is zero-padded: absmax 2 -> s = fp16(2/7) (0x3492),
+    # q = [2, -4, 1, 7, -3] and three padding codes of q = 0 (offset code 8):
+    # u = [10, 4, 9, 15, 5, 8, 8, 8] -> bytes 4a f9 85 88.
+    x = np.array([0.5, -1.0, 0.25, 2.0, -0.75], dtype=np.float32)
+    e = np.zeros(5, np.float32)
+    codes, scales = orc.quantize_pack(x, orc.params(4, 8), e)
+    assert scales.tolist() == [0x3492]
+    assert codes.tobytes() == bytes([0x4A, 0xF9, 0x85, 0x88])
+    assert e.tolist() == [-0.0712890625, 0.142578125, -0.03564453125, 0.00048828125, 0.10693359375]
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8, 12, 16])
+@pytest.mark.parametrize("rounding", [0, 1])
+def test_tail_block_equals_zero_padded_block(orc, bits, rounding):
+    # The reading for n mod B != 0: the last block behaves as if zero-padded
+    # to B elements (b >= 2).  So encoding n elements must give the same codes,
+    # scales and error as encoding the padded array, for every element < n.
+    rng = np.random.default_rng(bits + 10 * rounding)
+    B, n = 64, 5 * 64 + 23
+    x = (rng.standard_normal(n) * 1e-2).astype(np.float32)
+    xp = np.concatenate([x, np.zeros(64 - 23, np.float32)])
+    p = orc.params(bits, B, rounding, seed=3)
+    e, ep = np.zeros(n, np.float32), np.zeros(xp.size, np.float32)
+    c, sc = orc.quantize_pack(x, p, e)
+    cp, scp = orc.quantize_pack(xp, p, ep)
+    assert c.tobytes() == cp.tobytes() and np.array_equal(sc, scp)
+    assert np.array_equal(e.view(np.uint32), ep[:n].view(np.uint32))
+
+
+def test_one_bit_ignores_stochastic_rounding(orc):
+    # The reading for b = 1 with stochastic rounding: plain sign, as without it.
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal(1000) * 1e-3).astype(np.float32)
+    a = orc.quantize_pack(x, orc.params(1, 128, orc.RTN), np.zeros(1000, np.float32))
+    b = orc.quantize_pack(x, orc.params(1, 128, orc.SR, seed=5), np.zeros(1000, np.float32))
+    assert a[0].tobytes() == b[0].tobytes() and np.array_equal(a[1], b[1])
+
+
 @pytest.mark.parametrize("bits", [1, 2, 4, 8, 12, 16])
 def test_packing_matches_numpy_packbits(orc, bits):
     # Build blocks whose codes are known without the oracle: s = 2^-3 (exact in
