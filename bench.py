@@ -49,18 +49,29 @@ DEC_BYTES_PER_ELEM = W_RANKS * (BITS / 8 + 2 / BLOCK) + 4 + 4 + BITS / 8 + 2 / B
 NCU_TRAFFIC = {
     # profiles/launches_allreduce_w8_gpt1p3b.md: one full-size step, 1.3e9 elements per
     # encoder launch, 1.625e8 output elements per decoder launch
-    "encode": {"src": "e6b296c71fd8794b", "bytes_per_elem": (7.811851e9 + 5.820600e9) / 1.3e9},
-    "decode": {"src": "e6b296c71fd8794b", "bytes_per_elem": (1.320743e9 + 0.6848137e9) / 1.625e8},
+    "encode": {"src": "43d43c62a6a8129e", "bytes_per_elem": (7.811851e9 + 5.820600e9) / 1.3e9},
+    "decode": {"src": "43d43c62a6a8129e", "bytes_per_elem": (1.320743e9 + 0.6848137e9) / 1.625e8},
 }
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and with whitespace collapsed, so that a
+    comment edit does not invalidate measured traffic figures (the kernel
+    sources hold no comment markers inside string literals)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_src_hash() -> str:
+    """Hash of the kernel sources' code (comments and layout ignored)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_gradient_communication_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
