@@ -611,8 +611,10 @@ def run_workload(args):
         for _ in range(warm):
             step()
         t = _timed(torch, step, K, flush)
-        algo = wl.n * 2 * (4 + wl.bits / 8 + 2 / wl.block)
-        extra = {"l2": "flushed between timed iterations (256 MB write, then 256 MB read)"}
+        # one pass: read x, write codes + scales and the dequantised fp32 result
+        algo = wl.n * (4 + wl.bits / 8 + 2 / wl.block + 4)
+        extra = {"l2": "flushed between timed iterations (256 MB write, then 256 MB read)",
+                 "passes": "one (encoder with fused dequantisation)"}
     elif args.workload == "bucket25mb_f32":
         # one 25 MiB fusion bucket per call: the encoder entry point directly
         xs = [synth.gradients(wl.kind, wl.n, t, **wl.params) for t in range(10)]

@@ -285,6 +285,27 @@ bitscom_status bitscom_roundtrip(const void* x, bitscom_dtype dt, int64_t n, flo
 {
     if (n > 0 && !deq_out) return BITSCOM_EINVAL;
     if (deq_out && !aligned(deq_out, 32)) return BITSCOM_EALIGN;
+    if (!err && p && p->hadamard == 0 && n > 0) {
+        // one pass: codes, scales and fl(s*q) from the same registers
+        const bitscom_status chk = bitscom::check_encode(x, dt, n, err, p, codes_tmp, scales_tmp);
+        if (chk != BITSCOM_OK) return chk;
+        bitscom::EncArgs a;
+        a.x = x;
+        a.err = nullptr;
+        a.n = n;
+        a.log2B = log2_block(p->block);
+        a.nb = (n + p->block - 1) / p->block;
+        a.codes = static_cast<uint8_t*>(codes_tmp);
+        a.scales = scales_tmp;
+        a.keys = bitscom::philox_keys(p->seed, p->philox_stream);
+        a.index_offset = p->index_offset;
+        a.hadamard = 0;
+        a.deq = deq_out;
+        const cudaError_t e = bitscom::launch_roundtrip(a, dt == BITSCOM_F32 ? 0 : 1, p->bits,
+                                                        p->rounding == BITSCOM_SR,
+                                                        static_cast<cudaStream_t>(cuda_stream));
+        if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
     bitscom_status s = bitscom_quantize_pack(x, dt, n, err, p, codes_tmp, scales_tmp, cuda_stream);
     if (s != BITSCOM_OK || n == 0) return s;
     return bitscom_unpack_dequant(codes_tmp, scales_tmp, n, p, 1.0f, BITSCOM_F32, deq_out, cuda_stream);

@@ -216,7 +216,8 @@ __device__ __forceinline__ void load_row16(const EncArgs& a, int row, RowIn16<IN
     }
 }
 
-template <int IN, int BITS, bool EF, bool SR>
+// DEQ: also write fl(s*q) to a.deq (the one-pass roundtrip).
+template <int IN, int BITS, bool EF, bool SR, bool DEQ>
 __global__ void __launch_bounds__(kThreads16, 3) encode16_kernel(const EncArgs a)
 {
     __shared__ float red[2][kThreads16 / 32];
@@ -301,6 +302,21 @@ __global__ void __launch_bounds__(kThreads16, 3) encode16_kernel(const EncArgs a
         }
         if (team.lane == 0 && blk < a.nb) a.scales[blk] = __half_as_ushort(sh);
 
+        if constexpr (DEQ) {
+            // fl(s*q): exact for b <= 12, one rounding at b = 16, as in the decoders
+            float d0[8], d1[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) { d0[j] = __fmul_rn(s, q0[j]); d1[j] = __fmul_rn(s, q1[j]); }
+            if (valid == 16) {
+                st8_f32(a.deq + e0, d0);
+                st8_f32(a.deq + e0 + 8, d1);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (j < valid) a.deq[e0 + j] = j < 8 ? d0[j] : d1[j - 8];
+            }
+        }
+
         if constexpr (EF) {
             float f0[8], f1[8];
 #pragma unroll
@@ -320,7 +336,7 @@ __global__ void __launch_bounds__(kThreads16, 3) encode16_kernel(const EncArgs a
     }
 }
 
-template <int IN, int BITS, bool EF, bool SR>
+template <int IN, int BITS, bool EF, bool SR, bool DEQ = false>
 static cudaError_t run_encode16(const EncArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};
@@ -330,12 +346,12 @@ static cudaError_t run_encode16(const EncArgs& a, cudaStream_t st)
         int dev = 0, occ = 0, sms = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode16_kernel<IN, BITS, EF, SR>, kThreads16, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode16_kernel<IN, BITS, EF, SR, DEQ>, kThreads16, 0);
         c = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
         cap.store(c, std::memory_order_relaxed);
     }
     const int grid = (int)(rows < c ? rows : c);
-    encode16_kernel<IN, BITS, EF, SR><<<grid, kThreads16, 0, st>>>(a);
+    encode16_kernel<IN, BITS, EF, SR, DEQ><<<grid, kThreads16, 0, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -381,6 +397,31 @@ static cudaError_t encode_bits(const EncArgs& a, bool sr, cudaStream_t st)
     } else {
         if (ef) return sr ? run_encode<IN, BITS, true, true>(a, st) : run_encode<IN, BITS, true, false>(a, st);
         return sr ? run_encode<IN, BITS, false, true>(a, st) : run_encode<IN, BITS, false, false>(a, st);
+    }
+}
+
+template <int IN, int BITS>
+static cudaError_t roundtrip_bits(const EncArgs& a, bool sr, cudaStream_t st)
+{
+    if (!encode16_fits(a, BITS)) return cudaErrorNotSupported;
+    if constexpr (BITS == 1) {
+        return run_encode16<IN, 1, false, false, true>(a, st);
+    } else {
+        return sr ? run_encode16<IN, BITS, false, true, true>(a, st) : run_encode16<IN, BITS, false, false, true>(a, st);
+    }
+}
+
+template <int IN>
+static cudaError_t roundtrip_dispatch(const EncArgs& a, int bits, bool sr, cudaStream_t st)
+{
+    if (a.err != nullptr || a.deq == nullptr) return cudaErrorNotSupported;
+    switch (bits) {
+    case 1: return roundtrip_bits<IN, 1>(a, sr, st);
+    case 2: return roundtrip_bits<IN, 2>(a, sr, st);
+    case 4: return roundtrip_bits<IN, 4>(a, sr, st);
+    case 8: return roundtrip_bits<IN, 8>(a, sr, st);
+    case 16: return roundtrip_bits<IN, 16>(a, sr, st);
+    default: return cudaErrorNotSupported;
     }
 }
 

@@ -52,6 +52,7 @@ struct EncArgs {
     PhiloxKeys keys;        // stochastic rounding: philox_keys(seed, stream)
     uint64_t index_offset;
     int hadamard;           // 0 or the transform block H
+    float* deq = nullptr;   // fused roundtrip only: fl(s*q) as fp32 [n]
 };
 
 constexpr int kMaxRanks = 64;
@@ -99,6 +100,17 @@ inline cudaError_t launch_decode(const DecArgs& a, int bits_in, int bits_out, bo
     if (a.W == 8) return launch_decode_w8(a, bits_in, bits_out, sr, st);
     return a.W < 8 ? launch_decode_few(a, bits_in, bits_out, sr, st)
                    : launch_decode_many(a, bits_in, bits_out, sr, st);
+}
+
+// Quantise then dequantise in one pass (no error feedback, no rotation):
+// codes, scales and a.deq = fl(s*q).  cudaErrorNotSupported when the
+// arguments do not fit the one-pass kernel (the caller then runs the encoder
+// and the all-gather-side decode).
+cudaError_t launch_roundtrip_f32(const EncArgs& a, int bits, bool sr, cudaStream_t st);
+cudaError_t launch_roundtrip_bf16(const EncArgs& a, int bits, bool sr, cudaStream_t st);
+inline cudaError_t launch_roundtrip(const EncArgs& a, int dtype, int bits, bool sr, cudaStream_t st)
+{
+    return dtype == 0 ? launch_roundtrip_f32(a, bits, sr, st) : launch_roundtrip_bf16(a, bits, sr, st);
 }
 
 // Weight-difference quantisation: a.x = weights, a.err = reference (in/out).

@@ -190,8 +190,10 @@ bitscom_status bitscom_qwd_apply(const void* codes, const uint16_t* scales, int6
 
 /*
  * Quantise then dequantise (the simulate_quantization mode of "Implemented
- * Features"): the encoder into caller scratch codes_tmp / scales_tmp, then the
- * single-rank decoder into deq_out.  deq_out may alias x when dt == F32.
+ * Features"): the codes and scales go to caller scratch codes_tmp /
+ * scales_tmp and fl(s*q) to deq_out.  Without error feedback and rotation the
+ * encoder writes all three in one pass; otherwise the encoder runs, then the
+ * single-rank decoder.  deq_out may alias x when dt == F32.
  */
 bitscom_status bitscom_roundtrip(const void* x, bitscom_dtype dt, int64_t n, float* err,
                                  const bitscom_qparams* p, void* codes_tmp,

@@ -308,6 +308,45 @@ def test_roundtrip_matches_oracle(dt, bits):
     assert np.array_equal(eg.cpu().numpy().view(np.uint32), e_ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("bits", BITS)
+@pytest.mark.parametrize("rounding", ["rtn", "sr"])
+@pytest.mark.parametrize("block", [8, 32, 128, 4096])
+def test_roundtrip_without_feedback_matches_oracle(dt, bits, rounding, block):
+    # Without error feedback the roundtrip runs in one pass (codes, scales and
+    # fl(s*q) from the same registers) where the layout allows it (B >= 16,
+    # b != 12); the result, the codes and the scales must be the oracle's.
+    torch, bc = need_gpu()
+    sr = rounding == "sr"
+    for k, n in enumerate((3 * 4096 + 5, 16, 4096 + 40)):
+        x, _ = _inputs(n, dt, bits * 17 + block + k)
+        xh = x if dt == "f32" else bf16_bits_of(torch, x)
+        xg = torch.from_numpy(xh if dt == "f32" else xh.view(np.int16)).cuda()
+        if dt == "bf16":
+            xg = xg.view(torch.bfloat16)
+        p = bc.QParams(bits, block, bc.SR if sr else bc.RTN, seed=21, index_offset=8 * k + 2)
+        codes, scales = bc.alloc_codes(n, p)
+        deq = bc.roundtrip(xg, p, codes_tmp=codes, scales_tmp=scales)
+        c_ref, s_ref, d_ref = O.roundtrip(xh, O.params(bits, block, O.SR if sr else O.RTN, seed=21,
+                                                       index_offset=8 * k + 2))
+        torch.cuda.synchronize()
+        assert codes.cpu().numpy().tobytes() == c_ref.tobytes(), f"n={n}"
+        assert np.array_equal(scales.cpu().numpy().view(np.uint16), s_ref), f"n={n}"
+        assert np.array_equal(deq.cpu().numpy().view(np.uint32), d_ref.view(np.uint32)), f"n={n}"
+
+
+@pytest.mark.parametrize("bits", [1, 2, 8, 16])
+def test_roundtrip_in_place_all_widths(bits):
+    torch, bc = need_gpu()
+    n = 4096 * 2 + 19
+    x, _ = _inputs(n, "f32", 91 + bits)
+    xg = torch.from_numpy(x.copy()).cuda()
+    p = bc.QParams(bits, 64, bc.SR, seed=4)
+    bc.roundtrip(xg, p, deq_out=xg)
+    _, _, d_ref = O.roundtrip(x, O.params(bits, 64, O.SR, seed=4))
+    assert np.array_equal(xg.cpu().numpy().view(np.uint32), d_ref.view(np.uint32))
+
+
 def test_roundtrip_in_place():
     # deq_out may alias x for fp32 (the simulate-quantization mode)
     torch, bc = need_gpu()
