@@ -119,7 +119,9 @@ const char* bitscom_last_cuda_error(void);
  *   codes_out  packed_bytes(n) bytes; aligned to the per-thread store width:
  *              1 (b=1), 2 (b=2), 4 (b=4, 12), 8 (b=8), 16 (b=16) bytes.
  *   scales_out [num_blocks] fp16 bit patterns (2-byte aligned).
- * Buffers must not overlap.
+ * Buffers must not overlap.  Performance note: without error feedback a
+ * codes_out aligned to twice the store width (and blocks of >= 16) lets the
+ * encoder handle 16 elements per thread; the results are the same bits.
  */
 bitscom_status bitscom_quantize_pack(const void* x, bitscom_dtype dt, int64_t n, float* err,
                                      const bitscom_qparams* p, void* codes_out,
@@ -146,6 +148,9 @@ bitscom_status bitscom_quantize_pack(const void* x, bitscom_dtype dt, int64_t n,
  *   codes_out, scales_out   as in the encoder, for p_out.
  * The decoder has kernels for bits_out in {none, bits_in} and for the
  * two-level pair (8 -> 4); other pairs return BITSCOM_EUNSUPPORTED.
+ * Performance note: for W = 8 and 4 -> 4 bits, 8-byte aligned codes_in and
+ * codes_out (and blocks of >= 16) let the decoder handle 16 elements per
+ * thread; the results are the same bits.
  */
 bitscom_status bitscom_unpack_dequant_reduce_requant(
     const void* const* codes_in, const uint16_t* const* scales_in, int32_t W, int64_t n,
