@@ -101,11 +101,19 @@ __global__ void __launch_bounds__(kThreads, 2) qwd_apply_kernel(const QwdApplyAr
     const int64_t rows = (n + kRow - 1) / kRow;
     Packed<BITS> cur;
     unsigned short cur_s = 0;
+    float nref[8];   // the next row's reference, loaded one row ahead with its codes
     auto load = [&](int64_t row) {
         const int64_t e0 = row * kRow + (int64_t)threadIdx.x * kPiece;
         if (e0 >= n) return;
         cur = load_codes<BITS>(a.codes, e0 >> 3);
         cur_s = __ldg(a.scales + (e0 >> a.log2B));
+        const int64_t rem = n - e0;
+        if (rem >= 8) {
+            ld8_f32(a.ref + e0, nref);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) nref[j] = (j < rem) ? a.ref[e0 + j] : 0.0f;
+        }
     };
     if ((int64_t)blockIdx.x < rows) load(blockIdx.x);
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -113,12 +121,8 @@ __global__ void __launch_bounds__(kThreads, 2) qwd_apply_kernel(const QwdApplyAr
         const int64_t rem = n - e0;
         const int valid = rem <= 0 ? 0 : (rem >= 8 ? 8 : (int)rem);
         float r[8];
-        if (valid == 8) {
-            ld8_f32(a.ref + e0, r);
-        } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) r[j] = (j < valid) ? a.ref[e0 + j] : 0.0f;
-        }
+        for (int j = 0; j < 8; ++j) r[j] = nref[j];
         uint32_t h[4];
         level_pairs<BITS>(cur, h);
         if (row + gridDim.x < rows) load(row + gridDim.x);
