@@ -273,6 +273,33 @@ def test_decoder_w8_alignment_paths(offset, sr):
                 assert np.array_equal(sm.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), tag
 
 
+@pytest.mark.parametrize("bin_blk,bout_blk", [(32, 512), (512, 32), (16, 4096), (4096, 16)])
+def test_decoder_w8_mixed_blocks(bin_blk, bout_blk):
+    # Eight ranks of 4-bit codes requantised to 4 bits with a different block
+    # size on each side (the 16-elements-per-thread decoder handles both).
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(bin_blk * 3 + bout_blk)
+    W = 8
+    for n in (4 * 4096 + 48, 4096):
+        ins = [_random_codes(rng, n, 4, bin_blk) for _ in range(W)]
+        cin = [torch.from_numpy(c).cuda() for c, _ in ins]
+        sin = [torch.from_numpy(sc.view(np.int16)).cuda() for _, sc in ins]
+        e2 = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+        e2_g = torch.from_numpy(e2.copy()).cuda()
+        pout = bc.QParams(4, bout_blk, bc.RTN, philox_stream=1)
+        sm, co, so = bc.unpack_dequant_reduce_requant(cin, sin, n, bc.QParams(4, bin_blk), sum_out=True,
+                                                      err2=e2_g, p_out=pout)
+        torch.cuda.synchronize()
+        e2_ref = e2.copy()
+        s_ref, c_ref, sc_ref = O.unpack_dequant_reduce_requant(
+            [c for c, _ in ins], [sc for _, sc in ins], n, O.params(4, bin_blk), True, e2_ref,
+            O.params(4, bout_blk, philox_stream=1))
+        assert np.array_equal(sm.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), f"n={n}"
+        assert co.cpu().numpy().tobytes() == c_ref.tobytes(), f"n={n}"
+        assert np.array_equal(so.cpu().numpy().view(np.uint16), sc_ref), f"n={n}"
+        assert np.array_equal(e2_g.cpu().numpy().view(np.uint32), e2_ref.view(np.uint32)), f"n={n}"
+
+
 def test_decoder_requant_without_sum_output():
     torch, bc = need_gpu()
     rng = np.random.default_rng(11)
