@@ -516,6 +516,31 @@ def test_qwd_matches_oracle_over_steps(dt, bits, block, rounding):
         assert np.array_equal(wout.view(torch.int16).cpu().numpy().view(np.uint16), w_ref), f"step {t}"
 
 
+@pytest.mark.parametrize("wout", ["none", "f32"])
+def test_qwd_apply_weight_outputs(wout):
+    # The receiver's apply without a weight copy and with an fp32 one (the
+    # bf16 copy is covered above); the reference advances the same way.
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(7 + len(wout))
+    n, bits, block = 2 * 4096 + 136, 4, 128
+    w = rng.standard_normal(n).astype(np.float32)
+    ref_s = torch.from_numpy(w.copy()).cuda()
+    ref_r = torch.from_numpy(w.copy()).cuda()
+    h_ref_s, h_ref_r = w.copy(), w.copy()
+    w2 = (w + np.float32(1e-3) * rng.standard_normal(n).astype(np.float32)).astype(np.float32)
+    p = bc.QParams(bits, block)
+    po = O.params(bits, block)
+    codes, scales = bc.qwd_encode(torch.from_numpy(w2).cuda(), ref_s, p)
+    out = torch.empty(n, dtype=torch.float32, device="cuda") if wout == "f32" else None
+    bc.qwd_apply(codes, scales, n, p, ref_r, out)
+    torch.cuda.synchronize()
+    c_ref, s_ref = O.qwd_encode(w2, h_ref_s, po)
+    w_ref = O.qwd_apply(c_ref, s_ref, n, po, h_ref_r, O.F32)
+    assert np.array_equal(ref_r.cpu().numpy().view(np.uint32), h_ref_r.view(np.uint32))
+    if out is not None:
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), w_ref.view(np.uint32))
+
+
 @pytest.mark.parametrize("bits", [2, 4, 16])
 def test_decoder_maximum_ranks(bits):
     # W = 64, the largest rank count the ABI accepts (eight groups of eight in
