@@ -88,7 +88,13 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
 #pragma unroll
             for (int j = 0; j < 8; ++j) v[j] = __fadd_rn(v[j], cur.e[j]);
         }
-        // prefetch: row `ahead` reuses this buffer; its loads overlap the arithmetic
+        // prefetch: row `ahead` reuses this buffer; its loads overlap the arithmetic.
+        // The memory-bound encoders (error feedback, round to nearest, no
+        // rotation) first line up the CTA's warps, so that a row's loads reach
+        // DRAM together: 0.956 -> 0.987 of measured HBM for bf16 + EF, 4-bit,
+        // block 128.  Issue-bound variants (stochastic rounding, Hadamard,
+        // no error feedback) measured slower with the barrier.
+        if constexpr (EF && !SR && !HAD) __syncthreads();
         if (ahead < rows) load_row<IN, EF>(a, ahead, cur);
 
         // block statistic: absmax (b >= 2) or tree sum of |v| (b = 1)
