@@ -49,8 +49,8 @@ DEC_BYTES_PER_ELEM = W_RANKS * (BITS / 8 + 2 / BLOCK) + 4 + 4 + BITS / 8 + 2 / B
 NCU_TRAFFIC = {
     # profiles/launches_allreduce_w8_gpt1p3b.md: one full-size step, 1.3e9 elements per
     # encoder launch, 1.625e8 output elements per decoder launch
-    "encode": {"src": "5ab986303c231718", "bytes_per_elem": (7.811835e9 + 5.820603e9) / 1.3e9},
-    "decode": {"src": "5ab986303c231718", "bytes_per_elem": (1.321300e9 + 0.6835996e9) / 1.625e8},
+    "encode": {"src": "e0217c5eb1d137e2", "bytes_per_elem": (7.800326e9 + 5.807384e9) / 1.3e9},
+    "decode": {"src": "e0217c5eb1d137e2", "bytes_per_elem": (1.321209e9 + 0.6836558e9) / 1.625e8},
 }
 
 
