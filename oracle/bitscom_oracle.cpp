@@ -249,9 +249,10 @@ static uint16_t block_scale(const float* absv, int B, int n_valid, int bits)
 
 /* Integer code q of one value v under scale s (fp32 value of the fp16 scale).
  * b >= 2, round half to even : q = clamp(rint(v/s), -Qmax, Qmax)
- * b >= 2, stochastic         : t = v/s, f = floor(t), p = t - f,
- *                              u = (r mod 2^23) * 2^-23 with r the element's
- *                              Philox word, q = clamp(f + [u < p], +-Qmax)
+ * b >= 2, stochastic         : t = v/s, f = floor(t), p = t - f (exact,
+ *                              not rounded to fp32), u = (r mod 2^23) * 2^-23
+ *                              with r the element's Philox word,
+ *                              q = clamp(f + [u < p], +-Qmax)
  * s == 0 gives q = 0 (reading: an all-zero or underflowed block).
  * b == 1 : q = +1 if v >= 0 else -1 (reading: +0 and -0 both map to +1; the
  *          rounding mode is ignored, the 1-bit code is a deterministic sign). */
@@ -269,8 +270,11 @@ static int32_t quantize_value(float v, float s, const orc_params* p, uint64_t gi
         uint32_t r = orc_random_word(p->seed, p->philox_stream, gindex);
         float u = (float)(r & 0x7FFFFFu) * (1.0f / 8388608.0f);
         float f = floorf(t);
-        float frac = t - f;
-        q = f + ((u < frac) ? 1.0f : 0.0f);
+        /* Round up iff u < t - f, the fraction taken exactly: u < t - f is
+         * f + u < t, and f + u is exact in fp64 while |t| < 2^23 (an integer
+         * of at most 24 bits plus a multiple of 2^-23).  Larger t are
+         * integers (t = f), and the rounded f + u is never below f. */
+        q = f + (((double)f + (double)u < (double)t) ? 1.0f : 0.0f);
     }
     q = clampf(q, -qmax, qmax);
     return (int32_t)q;

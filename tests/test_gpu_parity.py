@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 import oracle as O
+from codec_util import codes_to_q, unpack_codes
 from gpu_util import Guarded, bf16_bits_of, need_gpu
 
 pytestmark = pytest.mark.gpu
@@ -172,6 +173,72 @@ def test_encoder_sr_tiny_elements(bits, absmax):
                     assert np.array_equal(scales, s_ref), tag
                     if ef:
                         assert np.array_equal(err.view(np.uint32), e_ref.view(np.uint32)), tag
+
+
+def _fraction_ties(bits, n, block, seed, stream, index_offset):
+    """Values whose stochastic rounding needs the exact fraction t - floor(t):
+    every block has scale 1 (its first element is Qmax, the rest lie inside
+    +-Qmax), and wherever the element's u = (r mod 2^23) 2^-23 lies in
+    (1/2, 3/4) its t is u + d - 1 for d = 2^-25, 0, -2^-25 in turn.  Those
+    round to q = 0, -1, -1: for d = 2^-25, 1 + t rounded to fp32 would be a
+    tie that goes to u itself (words from the oracle's Philox)."""
+    Q = (1 << (bits - 1)) - 1
+    rng = np.random.default_rng(bits * 7 + block)
+    x = rng.uniform(-Q, Q, n).astype(np.float32)
+    x[::block] = Q
+    m = O.random_words(seed, stream, index_offset, n) & 0x7FFFFF
+    sel = np.nonzero((m > 1 << 22) & (m < 3 << 21))[0]
+    sel = sel[sel % block != 0]
+    d = np.array([2.0 ** -25, 0.0, -2.0 ** -25])[np.arange(sel.size) % 3]
+    t = m[sel].astype(np.float64) * 2.0 ** -23 + d - 1.0
+    assert (t.astype(np.float32).astype(np.float64) == t).all()
+    x[sel] = t.astype(np.float32)
+    return x, sel, np.where(d > 0, 0, -1)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8, 12, 16])
+def test_sr_takes_the_exact_fraction(bits):
+    # Both encoder layouts (8 elements per thread with error feedback, 16
+    # without) and the stage-2 requantisation of the decoders (one rank and
+    # the eight-rank 4-bit decoder, whose summed zeros plus e2 give exactly
+    # these values) against the oracle and against the expected levels.
+    torch, bc = need_gpu()
+    n, B = 4096 * 3 + 64, 128
+    x, sel, q_exp = _fraction_ties(bits, n, B, 5, 0, 0)
+    p = bc.QParams(bits, B, bc.SR, seed=5)
+    for ef in (False, True):
+        e = np.zeros(n, np.float32)
+        codes, scales, err = _run_encode(torch, bc, x, "f32", n, p, e.copy() if ef else None)
+        e_ref = e.copy() if ef else None
+        c_ref, s_ref = O.quantize_pack(x, O.params(bits, B, O.SR, seed=5), e_ref)
+        assert codes.tobytes() == c_ref.tobytes() and np.array_equal(scales, s_ref), f"ef={ef}"
+        if ef:
+            assert np.array_equal(err.view(np.uint32), e_ref.view(np.uint32))
+        q = codes_to_q(unpack_codes(codes, bits, n), bits)
+        assert (q[sel] == q_exp).all()
+    # decoders: zero codes (scale 0) from W ranks, stage-2 error = x
+    for W, bin_ in ((1, bits), (8, 4)):
+        if W == 8 and bits != 4:
+            continue
+        x2, sel2, q2_exp = _fraction_ties(bits, n, B, 9, 1, 12)
+        zc, zs = O.quantize_pack(np.zeros(n, np.float32), O.params(bin_, B))
+        cin = [torch.from_numpy(zc).cuda() for _ in range(W)]
+        sin = [torch.from_numpy(zs.view(np.int16)).cuda() for _ in range(W)]
+        e2_g = torch.from_numpy(x2.copy()).cuda()
+        co, so = bc.alloc_codes(n, bc.QParams(bits, B))
+        pout = bc.QParams(bits, B, bc.SR, seed=9, index_offset=12, philox_stream=1)
+        bc.unpack_dequant_reduce_requant(cin, sin, n, bc.QParams(bin_, B), err2=e2_g, p_out=pout,
+                                         codes_out=co, scales_out=so)
+        torch.cuda.synchronize()
+        e2_ref = x2.copy()
+        _, c_ref, sc_ref = O.unpack_dequant_reduce_requant(
+            [zc] * W, [zs] * W, n, O.params(bin_, B), True, e2_ref,
+            O.params(bits, B, O.SR, seed=9, index_offset=12, philox_stream=1))
+        got = co.cpu().numpy()
+        assert got.tobytes() == c_ref.tobytes() and np.array_equal(so.cpu().numpy().view(np.uint16), sc_ref)
+        assert np.array_equal(e2_g.cpu().numpy().view(np.uint32), e2_ref.view(np.uint32))
+        q = codes_to_q(unpack_codes(got, bits, n), bits)
+        assert (q[sel2] == q2_exp).all(), f"W={W}"
 
 
 def _random_codes(rng, n, bits, block, scale_sigma=1e-3):

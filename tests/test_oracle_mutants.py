@@ -26,7 +26,8 @@ MUTANTS = {
                            "for (int w = W - 1; w >= 0; --w) {\n            float s = orc_f16_to_f32"),
     "philox_multiplier": ("M0 = 0xD2511F53u", "M0 = 0xD2511F55u"),
     "philox_weyl": ("W1 = 0xBB67AE85u", "W1 = 0xBB67AE87u"),
-    "sr_flipped": ("q = f + ((u < frac) ? 1.0f : 0.0f);", "q = f + ((u > frac) ? 1.0f : 0.0f);"),
+    "sr_flipped": ("(double)f + (double)u < (double)t", "(double)f + (double)u > (double)t"),
+    "sr_fraction_rounded": ("(double)f + (double)u < (double)t", "u < t - f"),
     "offset_off_by_one": ("return (uint32_t)(q + (1 << (bits - 1)));", "return (uint32_t)(q + (1 << (bits - 1)) - 1);"),
     "mean_over_block": ("x = sum / (float)n_valid;", "x = sum / (float)B;"),
     "fp16_truncates": ("if (rem > half || (rem == half && (M & 1u))) M += 1;", ";"),

@@ -443,7 +443,7 @@ def test_sr_levels_are_neighbours_and_seed_dependent(orc):
 
 @pytest.mark.parametrize("absmax,tiny,q_expected", [
     (7.0, 2.0 ** -149, 1),      # s = 1: t = 2^-149 > 0 = u
-    (7.0, -2.0 ** -149, 0),     # floor(t) = -1, p = fl(1 - 2^-149) = 1 > u
+    (7.0, -2.0 ** -149, 0),     # floor(t) = -1, t - floor(t) = 1 - 2^-149 > 0 = u
     (7.0, 0.0, 0),
     (7.0, -0.0, 0),
     (10.5, 2.0 ** -149, 1),     # s = 1.5: 2^-149 / 1.5 rounds up to 2^-149
@@ -461,6 +461,29 @@ def test_sr_tiny_quotient_where_u_is_zero(orc, absmax, tiny, q_expected):
     assert scales[0] == np.float16(absmax / 7).view(np.uint16)
     q = codes_to_q(unpack_codes(codes, 4, 8), 4)
     assert q[0] == 7 and q[1] == q_expected
+
+
+def test_sr_compares_the_exact_fraction(orc):
+    # For -1/2 < t < 0 the fraction t - floor(t) = 1 + t can need more bits
+    # than fp32 holds; stochastic rounding compares u with the exact fraction.
+    # With u in (1/2, 3/4) and t = u + 2^-25 - 1 (in (-1/2, -1/4), a multiple
+    # of 2^-25), u < 1 + t, so t rounds up to 0 -- although 1 + t rounded to
+    # fp32 is a tie that goes to the even neighbour u itself.  t = u - 1 and
+    # t = u - 2^-25 - 1 stay at -1.  Scale 1 (absmax 1, 2-bit: Qmax = 1).
+    words = orc.random_words(5, 0, 0, 256)
+    m = words & 0x7FFFFF
+    idx = [int(i) for i in np.nonzero((m > 1 << 22) & (m < 3 << 21))[0][:3]]
+    assert len(idx) == 3
+    for h in idx:
+        u = float(words[h] & 0x7FFFFF) * 2.0 ** -23
+        for delta, q_expected in ((2.0 ** -25, 0), (0.0, -1), (-2.0 ** -25, -1)):
+            t = u + delta - 1.0
+            assert float(np.float32(t)) == t
+            x = np.array([1.0, t, 0, 0, 0, 0, 0, 0], np.float32)
+            codes, scales = orc.quantize_pack(x, orc.params(2, 8, orc.SR, seed=5, index_offset=h - 1))
+            assert scales[0] == np.float16(1.0).view(np.uint16)
+            q = codes_to_q(unpack_codes(codes, 2, 8), 2)
+            assert q[1] == q_expected, (h, u, delta)
 
 
 @pytest.mark.parametrize("bits,rounding", [(2, 1), (4, 0), (8, 1), (1, 0)])
