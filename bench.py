@@ -23,6 +23,7 @@ thread) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -547,6 +548,9 @@ def run_workload(args):
     _build.build()
     torch.cuda.set_device(0)
     wl = synth.WORKLOADS[args.workload]
+    if args.wl_n:
+        # a smaller case of the same kernels, for profilers
+        wl = dataclasses.replace(wl, n=args.wl_n)
     peak, peak_kind = measured_peak_gbs()
     l2_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")   # > 129 MB L2
     l2_clean = torch.ones(256 << 20, dtype=torch.uint8, device="cuda")
@@ -719,7 +723,8 @@ def run_workload(args):
             step()
         t = _timed(torch, step, K)
         algo = wl.n * (2 + 8 + wl.bits / 8 + 2 / wl.block)
-        extra = {"l2": "inputs larger than L2 (67 GB per step)", "buckets": 512, "streams": 2}
+        extra = {"l2": "inputs larger than L2 (67 GB per step)" if not args.wl_n else "one pass per step",
+                 "buckets": len(bc.plan_buckets(wl.n, 2, wl.block, wl.bucket_bytes)) - 1, "streams": 2}
     else:
         raise SystemExit(f"workload {args.workload}: use the default run")
     gbs = algo / t / 1e6
@@ -749,6 +754,8 @@ def main():
                     help="bits,block,rtn|sr: run one configuration of sweep_laplace_256m")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="another workload recipe from synth.WORKLOADS (one JSON line of its own)")
+    ap.add_argument("--wl-n", type=int, default=0,
+                    help="run --workload with this many elements instead (a small case for profilers)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
