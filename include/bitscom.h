@@ -23,7 +23,7 @@
  *           balanced binary tree over contiguous halves of the zero-padded
  *           block and divided by the number of real elements; q = +1 if
  *           v >= 0 (both zeros) else -1; the rounding mode is ignored.
- *   Stochastic rounding: t = v/s, f = floor(t), p = t - f (fp32), u =
+ *   Stochastic rounding: t = v/s, f = floor(t), p = t - f (exact), u =
  *           (r mod 2^23) * 2^-23 with r = word (i mod 4) of Philox4x32-10
  *           (counter = (i/4 low, i/4 high, philox_stream, 0), key = (seed low,
  *           seed high)), i = index_offset + element index; q = clamp(f +
