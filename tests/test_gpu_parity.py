@@ -505,6 +505,29 @@ def test_allgather_decode_matches_oracle(bits, block, out):
         assert np.array_equal(got, ref.view(np.uint32 if out == "f32" else np.uint16)), f"n={n} mul={mul}"
 
 
+@pytest.mark.parametrize("bits", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_allgather_decode_many_rows_per_cta(bits, out):
+    # More than eight rows per CTA (2,600 rows of 4096 over at most 456 CTAs),
+    # so that the bf16 decode's four-row register ring is refilled several
+    # times and wraps around a ragged last row.
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(bits + (7 if out == "bf16" else 0))
+    n = 2600 * 4096 + 77
+    codes, scales = _random_codes(rng, n, bits, 128)
+    cg = Guarded(torch, codes.size, fill=codes)
+    sg = Guarded(torch, 2 * scales.size, fill=scales)
+    og = Guarded(torch, (4 if out == "f32" else 2) * n)
+    dst = og.view(torch.float32 if out == "f32" else torch.bfloat16)
+    mul = float(np.float32(1 / 8))
+    bc.unpack_dequant(cg.view(torch.uint8), sg.view(torch.int16), n, bc.QParams(bits, 128), mul, out=dst)
+    torch.cuda.synchronize()
+    assert og.guards_intact()
+    ref = O.unpack_dequant(codes, scales, n, O.params(bits, 128), mul, O.F32 if out == "f32" else O.BF16)
+    assert np.array_equal(og.host(np.uint32 if out == "f32" else np.uint16),
+                          ref.view(np.uint32 if out == "f32" else np.uint16))
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("bits", [2, 4, 8])
 @pytest.mark.parametrize("H,block", [(8, 8), (32, 128), (128, 128), (128, 512), (256, 4096)])
