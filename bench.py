@@ -530,7 +530,7 @@ def _timed(torch, fn, K, flush=None):
     for _ in range(K):
         if flush is not None:
             flush()
-        else:
+        elif hasattr(torch.cuda, "_sleep"):
             # keep the device busy (~50 us) while the host marshals the call's
             # arguments, so that the start event fires only when the launch is
             # already queued (the flush does the same where there is one)
