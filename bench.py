@@ -50,8 +50,8 @@ DEC_BYTES_PER_ELEM = W_RANKS * (BITS / 8 + 2 / BLOCK) + 4 + 4 + BITS / 8 + 2 / B
 NCU_TRAFFIC = {
     # profiles/launches_allreduce_w8_gpt1p3b.md: one full-size step, 1.3e9 elements per
     # encoder launch, 1.625e8 output elements per decoder launch
-    "encode": {"src": "93b9a249b68223b3", "bytes_per_elem": (7.800278e9 + 5.807404e9) / 1.3e9},
-    "decode": {"src": "93b9a249b68223b3", "bytes_per_elem": (1.321171e9 + 0.6834938e9) / 1.625e8},
+    "encode": {"src": "a8b7bb700d05d2c4", "bytes_per_elem": (7.800289e9 + 5.807496e9) / 1.3e9},
+    "decode": {"src": "a8b7bb700d05d2c4", "bytes_per_elem": (1.321248e9 + 0.6836018e9) / 1.625e8},
 }
 
 

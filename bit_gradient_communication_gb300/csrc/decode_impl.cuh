@@ -339,8 +339,8 @@ __global__ void __launch_bounds__(kThreads16, 3) decode16_w8_kernel(const DecArg
         }
         Packed<4> c0, c1;
         float q0[8], q1[8];
-        quantize8<4, SR>(v0, s2, y2, rw0, c0, q0);
-        quantize8<4, SR>(v1, s2, y2, rw1, c1, q1);
+        quantize8<4, SR, false>(v0, s2, y2, rw0, c0, q0);
+        quantize8<4, SR, false>(v1, s2, y2, rw1, c1, q1);
         if (e0 < (a.nb_out << a.log2Bout))
             *reinterpret_cast<uint2*>(a.codes_out + (e0 >> 1)) = make_uint2(c0.w[0], c1.w[0]);
         if (team.lane == 0 && blk < a.nb_out) a.scales_out[blk] = __half_as_ushort(sh);

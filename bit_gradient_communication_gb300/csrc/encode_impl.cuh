@@ -86,7 +86,12 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
         if constexpr (HAD) fwht8(v, a.hadamard);
         if constexpr (EF) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = __fadd_rn(v[j], cur.e[j]);
+            for (int i = 0; i < 4; ++i) {
+                const float2 t = __fadd2_rn(make_float2(v[2 * i], v[2 * i + 1]),
+                                            make_float2(cur.e[2 * i], cur.e[2 * i + 1]));
+                v[2 * i] = t.x;
+                v[2 * i + 1] = t.y;
+            }
         }
         // prefetch: row `ahead` reuses this buffer; its loads overlap the arithmetic.
         // The memory-bound encoders (error feedback, round to nearest, no
@@ -134,7 +139,12 @@ __global__ void __launch_bounds__(kThreads, 2) encode_kernel(const EncArgs a)
         if constexpr (EF) {
             float e[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) e[j] = feedback<BITS>(v[j], s, q[j]);
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = feedback2<BITS>(make_float2(v[2 * i], v[2 * i + 1]), s,
+                                                 make_float2(q[2 * i], q[2 * i + 1]));
+                e[2 * i] = f.x;
+                e[2 * i + 1] = f.y;
+            }
             if (valid == 8) {
                 st8_f32(a.err + e0, e);
             } else {
