@@ -46,12 +46,15 @@ DEC_BYTES_PER_ELEM = W_RANKS * (BITS / 8 + 2 / BLOCK) + 4 + 4 + BITS / 8 + 2 / B
 
 # DRAM traffic per element measured by ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum over the captured launch / its elements), valid only
-# while the kernel sources hash to `src`.  Filled from profiles/.
+# while the sources of the two kernels' translation units (TRAFFIC_SOURCES)
+# hash to `src`.  Filled from profiles/.
+TRAFFIC_SOURCES = ("launch.h", "codec.cuh", "encode_impl.cuh", "encode_bf16.cu", "decode_impl.cuh",
+                   "decode_w8.cu")
 NCU_TRAFFIC = {
     # profiles/launches_allreduce_w8_gpt1p3b.md: one full-size step, 1.3e9 elements per
     # encoder launch, 1.625e8 output elements per decoder launch
-    "encode": {"src": "a8b7bb700d05d2c4", "bytes_per_elem": (7.800289e9 + 5.807496e9) / 1.3e9},
-    "decode": {"src": "a8b7bb700d05d2c4", "bytes_per_elem": (1.321248e9 + 0.6836018e9) / 1.625e8},
+    "encode": {"src": "7824b74c713b748f", "bytes_per_elem": (7.800289e9 + 5.807496e9) / 1.3e9},
+    "decode": {"src": "7824b74c713b748f", "bytes_per_elem": (1.321248e9 + 0.6836018e9) / 1.625e8},
 }
 
 
@@ -65,14 +68,16 @@ def _code_only(text: str) -> str:
     return " ".join(text.split())
 
 
-def kernel_src_hash() -> str:
-    """Hash of the kernel sources' code (comments and layout ignored)."""
+def kernel_src_hash(files=None) -> str:
+    """Hash of the kernel sources' code (comments and layout ignored): all of
+    them, or the named files of the kernel directory."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_gradient_communication_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
-                h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
+    names = sorted(files) if files is not None else sorted(
+        f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    for f in names:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -267,10 +272,11 @@ def run_ours(args, rank, world, local_rank):
     enc_gbs = enc_bytes / enc_launch_s / 1e9
     dec_gbs = dec_bytes / dec_launch_s / 1e9
     src = kernel_src_hash()
+    tsrc = kernel_src_hash(TRAFFIC_SOURCES)
     tr = NCU_TRAFFIC.get("encode")
-    traffic = round(tr["bytes_per_elem"] * n) if tr and tr["src"] == src else None
+    traffic = round(tr["bytes_per_elem"] * n) if tr and tr["src"] == tsrc else None
     trd = NCU_TRAFFIC.get("decode")
-    dec_traffic = round(trd["bytes_per_elem"] * n / len(ar.chunks)) if trd and trd["src"] == src else None
+    dec_traffic = round(trd["bytes_per_elem"] * n / len(ar.chunks)) if trd and trd["src"] == tsrc else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
@@ -296,6 +302,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": K * (W + len(ar.chunks)),
         "clocks": clk,
         "kernel_src": src,
+        "traffic_src": tsrc,
     }
     if e2e:
         line["e2e"] = {"value": round(elems * 4 / (e2e["step_ms"] * 1e-3) / 1e9, 2), "unit": UNIT,
