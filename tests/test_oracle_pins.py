@@ -350,6 +350,21 @@ def test_random_word_uses_counter_layout(orc):
         assert orc.random_word(seed, stream, i) == int(out[i & 3])
 
 
+def test_stochastic_rounding_words_are_uniform(orc):
+    # Chi-square over 256 bins of 10^7 consecutive elements' words, for two
+    # seeds and both Philox streams: the top 8 of the 23 bits that form u and
+    # the lowest 8 bits.  255 degrees of freedom (mean 255, sd 22.6); the bound
+    # is 6 sd above the mean.
+    bound = 255 + 6 * np.sqrt(2 * 255)
+    for seed, stream in ((42, 0), (7, 1)):
+        w = orc.random_words(seed, stream, 12345, 10_000_000)
+        for bins in ((w & 0x7FFFFF) >> 15, w & 0xFF):
+            counts = np.bincount(bins.astype(np.int64), minlength=256)
+            e = w.size / 256
+            chi2 = float(((counts - e) ** 2 / e).sum())
+            assert chi2 < bound, (seed, stream, chi2)
+
+
 def _blocks(rng, kind, n):
     if kind == "normal":
         return rng.standard_normal(n).astype(np.float32)
