@@ -16,8 +16,9 @@ namespace bitscom {
 // element, so with one row ahead a decode of <= 8-bit codes into bf16 keeps
 // only ~6-12 KB of reads in flight per SM; a ring of four rows in registers
 // took it from 0.75-0.87 to 0.85-0.95 of measured HBM (2-, 4-, 8-bit codes,
-// 2^29 elements).  fp32 output (twice the writes, and the per-row barrier
-// below) measured best with one row ahead, as did 16-bit codes.
+// 2^29 elements; 1-bit codes take the same ring).  fp32 output (twice the
+// writes, and the per-row barrier below) measured best with one row ahead, as
+// did 16-bit codes; 12-bit codes keep one row too.
 template <int BITS, int OUT>
 __host__ __device__ constexpr int dq_depth() { return (OUT == 1 && BITS <= 8) ? 4 : 1; }
 
