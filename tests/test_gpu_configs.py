@@ -1,15 +1,16 @@
 """The five workloads at their full sizes on the GPU, checked against the CPU
-oracle.  Workloads the oracle finishes in seconds are compared whole; the
-large ones on block-aligned windows (first and last blocks, chunk and bucket
-boundaries, random positions): every block is independent given its global
-element index, so a window is a complete oracle problem of its own.
-The oracle always starts from its own state (zero error buffers) -- no
-oracle input comes from the CUDA path."""
+oracle on every element.  The small ones are compared in one piece; the large
+ones are streamed through the oracle in block-aligned slices on every host
+core (tests/whole_check.py): every block is independent given its global
+element index, so a slice is a complete oracle problem of its own.  The
+oracle always starts from its own state (zero error buffers) -- no oracle
+input comes from the CUDA path."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as O
+import whole_check
 from gpu_util import need_gpu
 
 pytestmark = pytest.mark.gpu
@@ -21,23 +22,6 @@ def _bits16(x):
 
 def _host(x):
     return x.cpu().numpy() if x.dtype == torch.float32 else _bits16(x)
-
-
-def _windows(n, block, count, length_blocks, seed, must_blocks=()):
-    nb = (n + block - 1) // block
-    rng = np.random.default_rng(seed)
-    starts = {0, max(0, nb - length_blocks)}
-    for b in must_blocks:
-        for d in (-1, 0):
-            starts.add(min(max(0, b + d * length_blocks // 2), max(0, nb - length_blocks)))
-    starts |= set(int(v) for v in rng.integers(0, max(1, nb - length_blocks), count))
-    return [(b * block, min((b + length_blocks) * block, n), b) for b in sorted(starts)]
-
-
-def _codes_window(codes, bits, lo, hi, block):
-    b0 = lo // block
-    b1 = (hi + block - 1) // block
-    return codes[b0 * block * bits // 8: b1 * block * bits // 8]
 
 
 def test_roundtrip_1m_full():
@@ -78,87 +62,169 @@ def test_bucket25mb_ten_steps_full(bits):
     sched.close()
 
 
-def test_allreduce_w8_gpt1p3b_windows():
+def _f32(t):
+    return t.cpu().numpy()
+
+
+def _u16(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _u8(t):
+    return t.cpu().numpy()
+
+
+def test_allreduce_w8_gpt1p3b_whole_two_steps():
+    """Config 3 whole: 8 ranks x 1.3e9 bf16, two steps of the simulated
+    all-reduce with the bench's launches (8 encoders, 8 chunk decoders).  Every
+    element's codes, scale, error e' and stage-2 error e2' and every output code
+    and scale of both steps is compared with the oracle (step 2 starts from the
+    errors step 1 left, on both sides)."""
     _, bc = need_gpu()
     import bench
     from bit_gradient_communication_gb300 import synth
-    W, n = 8, bench.N_PER_RANK
+    W, n, B, b = 8, bench.N_PER_RANK, bench.BLOCK, bench.BITS
     ar = bench.AllReduceW8(torch, bc, synth, n, W, torch.device("cuda"))
     ar.encode()
     ar.decode()
+    first = {"err": [e.clone() for e in ar.err], "codes": [c.clone() for c in ar.codes],
+             "scales": [s.clone() for s in ar.scales], "err2": ar.err2.clone(),
+             "codes_out": ar.codes_out.clone(), "scales_out": ar.scales_out.clone()}
+    ar.encode()
+    ar.decode()
     torch.cuda.synchronize()
-    B = bench.BLOCK
-    bounds = [lo // B for (lo, _) in ar.chunks]
-    for lo, hi, b0 in _windows(n, B, 48, 64, 3, bounds):
+    second = {"err": ar.err, "codes": list(ar.codes), "scales": list(ar.scales), "err2": ar.err2,
+              "codes_out": ar.codes_out, "scales_out": ar.scales_out}
+    assert n % B == 0
+
+    def state(st, lo, hi):
+        return {"err": [_f32(e[lo:hi]) for e in st["err"]],
+                "codes": [_u8(c[lo * b // 8: hi * b // 8]) for c in st["codes"]],
+                "scales": [_u16(s[lo // B: hi // B]) for s in st["scales"]],
+                "err2": _f32(st["err2"][lo:hi]), "codes_out": _u8(st["codes_out"][lo * b // 8: hi * b // 8]),
+                "scales_out": _u16(st["scales_out"][lo // B: hi // B])}
+
+    def fetch(lo, hi):
+        return {"x": [_u16(x[lo:hi]) for x in ar.x], 1: state(first, lo, hi), 2: state(second, lo, hi)}
+
+    def check(lo, hi, d):
         m = hi - lo
-        enc = []
-        for w in range(W):
-            e = np.zeros(m, np.float32)
-            c_ref, s_ref = O.quantize_pack(_bits16(ar.x[w][lo:hi]), O.params(4, B), e)
-            enc.append((c_ref, s_ref))
-            assert _codes_window(ar.codes[w], 4, lo, hi, B).cpu().numpy().tobytes() == c_ref.tobytes()
-            assert np.array_equal(ar.scales[w][b0:b0 + len(s_ref)].cpu().numpy().view(np.uint16), s_ref)
-            assert np.array_equal(ar.err[w][lo:hi].cpu().numpy().view(np.uint32), e.view(np.uint32))
+        e = [np.zeros(m, np.float32) for _ in range(W)]
         e2 = np.zeros(m, np.float32)
-        _, co, so = O.unpack_dequant_reduce_requant([c for c, _ in enc], [s for _, s in enc], m,
-                                                    O.params(4, B), False, e2,
-                                                    O.params(4, B, index_offset=lo, philox_stream=1))
-        assert _codes_window(ar.codes_out, 4, lo, hi, B).cpu().numpy().tobytes() == co.tobytes()
-        assert np.array_equal(ar.scales_out[b0:b0 + len(so)].cpu().numpy().view(np.uint16), so)
-        assert np.array_equal(ar.err2[lo:hi].cpu().numpy().view(np.uint32), e2.view(np.uint32))
-    del ar
+        for step in (1, 2):
+            g = d[step]
+            enc = []
+            for w in range(W):
+                c, s = O.quantize_pack(d["x"][w], O.params(b, B, seed=1000 + w, index_offset=lo), e[w])
+                assert whole_check.same_bits(c, g["codes"][w]), f"step {step} rank {w} codes at {lo}"
+                assert whole_check.same_bits(s, g["scales"][w]), f"step {step} rank {w} scales at {lo}"
+                assert whole_check.same_bits(e[w], g["err"][w]), f"step {step} rank {w} e' at {lo}"
+                enc.append((c, s))
+            _, co, so = O.unpack_dequant_reduce_requant([c for c, _ in enc], [s for _, s in enc], m,
+                                                        O.params(b, B), False, e2,
+                                                        O.params(b, B, index_offset=lo, philox_stream=1))
+            assert whole_check.same_bits(co, g["codes_out"]), f"step {step} output codes at {lo}"
+            assert whole_check.same_bits(so, g["scales_out"]), f"step {step} output scales at {lo}"
+            assert whole_check.same_bits(e2, g["err2"]), f"step {step} e2' at {lo}"
+
+    checked = whole_check.run(whole_check.slices(n, 1 << 21), fetch, check)
+    assert checked == n
+    del ar, first, second
     torch.cuda.empty_cache()
 
 
-def test_gpt6p7b_2bit_buckets_windows():
+def test_gpt6p7b_2bit_buckets_whole_two_steps():
+    """Config 4 whole: 6.7e9 bf16, 2-bit block-64 stochastic rounding with
+    error feedback, 512 buckets of 25 MiB on two streams, two steps (step t
+    draws Philox words at global index t*n + i).  Every element's codes,
+    scale and e' of both steps is compared with the oracle."""
     _, bc = need_gpu()
     from bit_gradient_communication_gb300 import synth
     wl = synth.WORKLOADS["gpt6p7b_2bit_buckets"]
-    n = wl.n
+    n, b, B = wl.n, wl.bits, wl.block
     x = synth.gradients(wl.kind, n, wl.seed, dtype=torch.bfloat16, **wl.params)
     err = torch.zeros(n, device="cuda")
-    p = bc.QParams(wl.bits, wl.block, wl.rounding, seed=wl.sr_seed)
-    codes, scales = bc.alloc_codes(n, p)
+    codes, scales = bc.alloc_codes(n, bc.QParams(b, B))
     sched = bc.Scheduler(n_streams=2, bucket_bytes=wl.bucket_bytes)
-    sched.quantize_pack(x, p, err, codes, scales)
+    assert len(bc.plan_buckets(n, 2, B, wl.bucket_bytes)) - 1 == 512
+    p = lambda t: bc.QParams(b, B, wl.rounding, seed=wl.sr_seed, index_offset=t * n)
+    sched.quantize_pack(x, p(0), err, codes, scales)
     sched.wait(timeout_s=120)
-    starts = bc.plan_buckets(n, 2, wl.block, wl.bucket_bytes)
-    assert len(starts) - 1 == 512
-    bounds = [s // wl.block for s in starts[1:-1:37]] + [starts[-2] // wl.block]
-    for lo, hi, b0 in _windows(n, wl.block, 48, 128, 4, bounds):
-        e = np.zeros(hi - lo, np.float32)
-        c_ref, s_ref = O.quantize_pack(_bits16(x[lo:hi]),
-                                       O.params(wl.bits, wl.block, wl.rounding, seed=wl.sr_seed,
-                                                index_offset=lo), e)
-        assert _codes_window(codes, wl.bits, lo, hi, wl.block).cpu().numpy().tobytes() == c_ref.tobytes()
-        assert np.array_equal(scales[b0:b0 + len(s_ref)].cpu().numpy().view(np.uint16), s_ref)
-        assert np.array_equal(err[lo:hi].cpu().numpy().view(np.uint32), e.view(np.uint32))
+    first = (err.clone(), codes.clone(), scales.clone())
+    sched.quantize_pack(x, p(1), err, codes, scales)
+    sched.wait(timeout_s=120)
+    torch.cuda.synchronize()
     sched.close()
-    del x, err, codes, scales
+    assert n % B == 0
+
+    def fetch(lo, hi):
+        out = {"x": _u16(x[lo:hi])}
+        for step, (e, c, s) in ((0, first), (1, (err, codes, scales))):
+            out[step] = (_f32(e[lo:hi]), _u8(c[lo * b // 8: hi * b // 8]), _u16(s[lo // B: hi // B]))
+        return out
+
+    def check(lo, hi, d):
+        e = np.zeros(hi - lo, np.float32)
+        for step in (0, 1):
+            c, s = O.quantize_pack(d["x"], O.params(b, B, wl.rounding, seed=wl.sr_seed,
+                                                    index_offset=step * n + lo), e)
+            ge, gc, gs = d[step]
+            assert whole_check.same_bits(c, gc), f"step {step} codes at {lo}"
+            assert whole_check.same_bits(s, gs), f"step {step} scales at {lo}"
+            assert whole_check.same_bits(e, ge), f"step {step} e' at {lo}"
+
+    checked = whole_check.run(whole_check.slices(n, 1 << 22), fetch, check)
+    assert checked == n
+    del x, err, codes, scales, first
     torch.cuda.empty_cache()
 
 
-def test_sweep_laplace_256m_windows():
+SWEEP_BITS = (1, 2, 4, 8, 12, 16)
+SWEEP_BLOCKS = (32, 64, 128, 256, 1024, 4096)
+
+
+def test_sweep_laplace_256m_whole():
+    """Config 5 whole: 268,435,456 fp32 Laplace(0, 1e-3), every bits x block x
+    {RTN, SR} cell (72).  Per cell the encoder (codes, scales) and the W=1
+    decoder the sweep times (fl(s*q) as the rank sum) are compared with the
+    oracle on every element; the one-pass roundtrip entry point must give the
+    same codes, scales and values bit for bit."""
     _, bc = need_gpu()
     from bit_gradient_communication_gb300 import synth
     wl = synth.WORKLOADS["sweep_laplace_256m"]
     n = wl.n
     x = synth.gradients(wl.kind, n, wl.seed, **wl.params)
+    xh = x.cpu().numpy()
     deq = torch.empty(n, device="cuda")
-    for bits in (1, 2, 4, 8, 12, 16):
-        for block in (32, 64, 128, 256, 1024, 4096):
+    rt = torch.empty(n, device="cuda")
+    total = 0
+    for bits in SWEEP_BITS:
+        for block in SWEEP_BLOCKS:
             for rounding in (bc.RTN, bc.SR):
                 p = bc.QParams(bits, block, rounding, seed=wl.sr_seed)
-                codes, scales = bc.alloc_codes(n, p)
-                bc.roundtrip(x, p, codes_tmp=codes, scales_tmp=scales, deq_out=deq)
+                codes, scales = bc.quantize_pack(x, p)
+                bc.unpack_dequant_reduce_requant([codes], [scales], n, p, sum_out=deq)
+                c2, s2 = bc.alloc_codes(n, p)
+                bc.roundtrip(x, p, codes_tmp=c2, scales_tmp=s2, deq_out=rt)
                 torch.cuda.synchronize()
-                for lo, hi, b0 in _windows(n, block, 6, max(1, 4096 // block), bits * 100 + block):
-                    c_ref, s_ref, d_ref = O.roundtrip(
-                        x[lo:hi].cpu().numpy(), O.params(bits, block, rounding, seed=wl.sr_seed, index_offset=lo))
-                    tag = f"b={bits} B={block} r={rounding} lo={lo}"
-                    assert _codes_window(codes, bits, lo, hi, block).cpu().numpy().tobytes() == c_ref.tobytes(), tag
-                    assert np.array_equal(scales[b0:b0 + len(s_ref)].cpu().numpy().view(np.uint16), s_ref), tag
-                    assert np.array_equal(deq[lo:hi].cpu().numpy().view(np.uint32), d_ref.view(np.uint32)), tag
+                tag = f"b={bits} B={block} r={rounding}"
+                assert torch.equal(c2, codes) and torch.equal(s2, scales), tag
+                assert torch.equal(rt.view(torch.int32), deq.view(torch.int32)), tag
+                del c2, s2
+
+                def fetch(lo, hi):
+                    return (_u8(codes[lo * bits // 8: hi * bits // 8]), _u16(scales[lo // block: hi // block]),
+                            _f32(deq[lo:hi]))
+
+                def check(lo, hi, d):
+                    op = O.params(bits, block, rounding, seed=wl.sr_seed, index_offset=lo)
+                    c, s = O.quantize_pack(xh[lo:hi], op)
+                    assert whole_check.same_bits(c, d[0]), f"{tag} codes at {lo}"
+                    assert whole_check.same_bits(s, d[1]), f"{tag} scales at {lo}"
+                    assert whole_check.same_bits(O.unpack_dequant(c, s, hi - lo, op), d[2]), f"{tag} values at {lo}"
+
+                total += whole_check.run(whole_check.slices(n, 1 << 22), fetch, check)
                 del codes, scales
-    del x, deq
+    assert total == n * len(SWEEP_BITS) * len(SWEEP_BLOCKS) * 2
+    del x, deq, rt
     torch.cuda.empty_cache()
