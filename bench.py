@@ -15,9 +15,12 @@ HBM copy bandwidth.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Under torchrun (N > 1) every rank runs its own replica of the workload on its
-own GPU (the ranks are independent problems): value = all ranks' elements /
-the slowest rank's time.  --impl reference times the CPU oracle (single
+Under torchrun (N > 1) every GPU is one rank of the real low-bit all-reduce
+(W = N ranks of 1.3e9 bf16 elements each): its encoder, an all-to-all of the
+packed chunks over NCCL, the decoder of its own chunk and an all-gather of the
+requantised chunks; value = all ranks' elements / the slowest rank's step
+time.  --replicas instead runs N independent copies of the single-GPU
+simulation.  --impl reference times the CPU oracle (single
 thread) on a bounded sample of the same workload.
 """
 from __future__ import annotations
@@ -311,6 +314,114 @@ def run_ours(args, rank, world, local_rank):
     if cpu:
         line["cpu_baseline"] = cpu
         line["cpu_baseline_all_cores"] = cpu_all
+    print(json.dumps(line), flush=True)
+
+
+def sharded_rank(torch, bc, synth, sharded, n, rank, world, device, bucket_bytes, codec=None, exchange=None,
+                 grad=None):
+    """One rank of the real multi-GPU all-reduce of the headline workload: this
+    rank's 1.3e9-element bf16 gradient (N(0, 1e-3^2), seed 1000 + rank), 4-bit
+    block-128 round-to-nearest encoder with error feedback, stage-2
+    requantisation with error feedback, buckets of bucket_bytes."""
+    if grad is None:
+        grad = synth.gradients("normal", n, 1000 + rank, dtype=torch.bfloat16, device=device, sigma=1e-3)
+    ar = sharded.LowBitAllReduce(n, torch.bfloat16, bc.QParams(BITS, BLOCK, bc.RTN, seed=1000 + rank),
+                                 bc.QParams(BITS, BLOCK, bc.RTN, philox_stream=1), device=device,
+                                 bucket_bytes=bucket_bytes, codec=codec, exchange=exchange)
+    return ar, grad
+
+
+def run_sharded(args, rank, world, local_rank):
+    """N > 1: every GPU is one rank of the low-bit all-reduce (W = N): encode
+    its own gradient, all-to-all of the chunks over NCCL, decode-reduce-requant
+    of its own chunk, all-gather of the requantised chunks.  value = all ranks'
+    gradient elements (counted as fp32 bytes) / the slowest rank's step time."""
+    import torch
+    import torch.distributed as dist
+
+    import bit_gradient_communication_gb300 as bc
+    from bit_gradient_communication_gb300 import _build, sharded, synth
+
+    if rank == 0:
+        _build.build()
+    dist.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    n = args.n
+    ar, grad = sharded_rank(torch, bc, synth, sharded, n, rank, world, dev, args.bucket_mb << 20)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        ar(grad)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    for k in range(K):
+        ev[k][0].record(stream)
+        state = ar.send(grad)
+        ev[k][1].record(stream)            # every bucket's encoder is queued before this
+        ar.finish(ar.reduce(state))
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    t = torch.tensor([ev[0][0].elapsed_time(ev[K - 1][2]),
+                      sum(e[0].elapsed_time(e[1]) for e in ev) / K], device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    step_ms, enc_ms = float(t[0]) / K, float(t[1])
+
+    # end to end: pinned host gradient in, gathered requantised codes + scales out, every step
+    e2e = None
+    if not args.no_e2e:
+        host_g = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+        host_g.copy_(grad)
+        out_c = torch.empty(bc.packed_bytes(n, BITS, BLOCK), dtype=torch.uint8, device=dev)
+        out_s = torch.empty(bc.num_blocks(n, BLOCK), dtype=torch.int16, device=dev)
+        host_c = torch.empty(out_c.numel(), dtype=torch.uint8, pin_memory=True)
+        host_s = torch.empty(out_s.numel(), dtype=torch.int16, pin_memory=True)
+        steps = max(1, min(K, args.e2e_steps))
+        dist.barrier()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            grad.copy_(host_g, non_blocking=True)
+            ar(grad, out_codes=out_c, out_scales=out_s)
+            host_c.copy_(out_c, non_blocking=True)
+            host_s.copy_(out_s, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        te = torch.tensor([a.elapsed_time(b) / steps], device=dev)
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"step_ms": float(te), "h2d": n * 2, "d2h": host_c.numel() + host_s.numel() * 2}
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak_gbs()
+    enc_gbs = n * ENC_BYTES_PER_ELEM / (enc_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(world * n * 4 / (step_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "ranks": world, "elements_per_rank": n, "input_dtype": "bf16",
+                   "bits": BITS, "block": BLOCK, "rounding": "rtn", "error_feedback": "stage1+stage2",
+                   "buckets": len(ar.buckets), "bucket_bytes": args.bucket_mb << 20,
+                   "l2": "inputs larger than L2 (%.1f GB of gradient per rank)" % (n * 2 / 1e9),
+                   "parallelism": f"sharded low-bit all-reduce over NCCL, {world} ranks (all-to-all + all-gather)"},
+        "roofline": {"bound": "hbm", "kernel": "encode_kernel<bf16,4,ef,rtn> (all buckets of one step)",
+                     "achieved": round(enc_gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(enc_gbs / peak, 4),
+                     "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": n * ENC_BYTES_PER_ELEM,
+                     "launch_ms": round(enc_ms, 4)},
+        "gpu_launches": K * 2 * len(ar.buckets),
+        "clocks": clk, "kernel_src": kernel_src_hash(),
+    }
+    if e2e:
+        line["e2e"] = {"value": round(world * n * 4 / (e2e["step_ms"] * 1e-3) / 1e9, 2), "unit": UNIT,
+                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                       "ms_per_step": round(e2e["step_ms"], 3)}
     print(json.dumps(line), flush=True)
 
 
@@ -766,6 +877,9 @@ def main():
                     help="bits,block,rtn|sr: run one configuration of sweep_laplace_256m")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="another workload recipe from synth.WORKLOADS (one JSON line of its own)")
+    ap.add_argument("--replicas", action="store_true",
+                    help="N > 1: run N independent copies of the single-GPU simulation instead of the sharded all-reduce")
+    ap.add_argument("--bucket-mb", type=int, default=25, help="N > 1: fusion bucket size in MiB of bf16 gradient")
     ap.add_argument("--wl-n", type=int, default=0,
                     help="run --workload with this many elements instead (a small case for profilers)")
     args = ap.parse_args()
@@ -784,10 +898,16 @@ def main():
     if world > 1:
         import torch
         import torch.distributed as dist
+        # NCCL's communicator lines (ranks, devices) on stdout, for checking the ranks
+        os.environ.setdefault("NCCL_DEBUG", "INFO")
+        os.environ.setdefault("NCCL_DEBUG_SUBSYS", "INIT")
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        run_ours(args, rank, world, local_rank)
+        if world > 1 and not args.replicas:
+            run_sharded(args, rank, world, local_rank)
+        else:
+            run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

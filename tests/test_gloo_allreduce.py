@@ -1,14 +1,17 @@
 """The sharded low-bit all-reduce across real ranks, on the CPU (gloo).
 
-Each of W ranks encodes its own gradient (oracle codec, first-stage error
-feedback, per-rank stochastic-rounding seed), sends chunk c of its codes and
-scales to rank c (the all-to-all, done with point-to-point messages because
-gloo has no all-to-all), decodes the W chunks it received in rank order,
-requantises with its shard of the stage-2 error and all-gathers the
-requantised chunks (bitscom README, "Implemented Features": all-to-all ->
-local reduce -> all-gather; DeAR README: reduce-scatter + all-gather).  The
-gathered result and every error buffer must equal the single-process
-simulation with W arrays, which is what the GPU path computes.
+Each of W processes runs the package's multi-rank orchestration
+(bit_gradient_communication_gb300.sharded.LowBitAllReduce): it encodes its own
+gradient bucket by bucket (first-stage error feedback, per-rank
+stochastic-rounding seed), sends chunk c of its codes and scales to rank c
+(all_to_all_single), decodes the W chunks it received in rank order,
+requantises with its shard of the stage-2 error, all-gathers the requantised
+chunks and decodes the mean (bitscom README, "Implemented Features":
+all-to-all -> local reduce -> all-gather; DeAR README: reduce-scatter +
+all-gather).  The codec steps run in the CPU oracle here (tests/oracle_codec.py;
+the GPU version of this test, tests/test_gpu_sharded.py, runs libbitscom).  The
+gathered codes, scales, decoded mean and every error buffer must equal the
+single-process simulation of W ranks (tests/sharded_sim.py) over two steps.
 """
 import os
 import socket
@@ -18,6 +21,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 N, BITS, BLOCK, STEPS = 3 * 4096 + 640, 4, 128, 2
+BUCKET_BYTES = 16 * 1024          # 4096 fp32 elements: four buckets, the last one ragged
 
 
 def _free_port():
@@ -26,16 +30,6 @@ def _free_port():
     port = s.getsockname()[1]
     s.close()
     return port
-
-
-def _chunks(n, W, B):
-    nb = (n + B - 1) // B
-    cb = (nb + W - 1) // W
-    out = []
-    for c in range(W):
-        b0, b1 = c * cb, min((c + 1) * cb, nb)
-        out.append((b0 * B, min(b1 * B, n), b0, b1))
-    return out
 
 
 def _grad(rank, step):
@@ -52,114 +46,76 @@ def _worker(rank, W, port, outdir, drop=None, timeout_s=None):
     import sys
     from datetime import timedelta
     sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
     import torch
     import torch.distributed as dist
 
-    import oracle as O
+    import bit_gradient_communication_gb300 as bc
+    from bit_gradient_communication_gb300 import sharded
+    from oracle_codec import OracleCodec
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     kw = {"timeout": timedelta(seconds=timeout_s)} if timeout_s else {}
     dist.init_process_group("gloo", rank=rank, world_size=W, **kw)
-    chunks = _chunks(N, W, BLOCK)
-    lo, hi, b0, b1 = chunks[rank]
-    err = np.zeros(N, np.float32)
-    e2_shard = np.zeros(hi - lo, np.float32)
+    ar = sharded.LowBitAllReduce(N, torch.float32, bc.QParams(BITS, BLOCK, bc.SR, seed=1000 + rank),
+                                 bc.QParams(BITS, BLOCK, bc.SR, seed=77, philox_stream=1), device="cpu",
+                                 bucket_bytes=BUCKET_BYTES, codec=OracleCodec(),
+                                 exchange=sharded.Exchange(host_staging=(W == 3)))
     for step in range(STEPS):
         if drop is not None and drop == (rank, step):
             os._exit(0)
-        if drop is not None:
-            try:
-                _step(rank, W, step, chunks, err, e2_shard, outdir, O, torch, dist)
-            except RuntimeError as exc:
-                with open(os.path.join(outdir, f"failed{rank}.txt"), "w") as f:
-                    f.write(f"{step}\n{type(exc).__name__}: {exc}\n")
-                os._exit(0)
-            continue
-        _step(rank, W, step, chunks, err, e2_shard, outdir, O, torch, dist)
-    np.save(os.path.join(outdir, f"err{rank}.npy"), err)
+        g = torch.from_numpy(_grad(rank, step))
+        codes = torch.zeros(bc.packed_bytes(N, BITS, BLOCK), dtype=torch.uint8)
+        scales = torch.zeros(bc.num_blocks(N, BLOCK), dtype=torch.int16)
+        out = torch.empty(N)
+        try:
+            ar(g, out=out, mul=1.0 / W, out_codes=codes, out_scales=scales)
+        except RuntimeError as exc:
+            if drop is None:
+                raise
+            with open(os.path.join(outdir, f"failed{rank}.txt"), "w") as f:
+                f.write(f"{step}\n{type(exc).__name__}: {exc}\n")
+            os._exit(0)
+        np.savez(os.path.join(outdir, f"step{step}_rank{rank}.npz"), codes=codes.numpy(),
+                 scales=scales.numpy().view(np.uint16), out=out.numpy())
+    np.save(os.path.join(outdir, f"err{rank}.npy"), ar.err.numpy())
+    np.save(os.path.join(outdir, f"e2_{rank}.npy"), ar.err2[:ar.shard].numpy())
     dist.barrier()
     dist.destroy_process_group()
 
 
-def _step(rank, W, step, chunks, err, e2_shard, outdir, O, torch, dist):
-    """One all-reduce step of one rank: encode, all-to-all, reduce, all-gather."""
-    lo, hi, b0, b1 = chunks[rank]
-    g = _grad(rank, step)
-    p1 = O.params(BITS, BLOCK, O.SR, seed=1000 + rank, index_offset=step * N)
-    codes, scales = O.quantize_pack(g, p1, err)
-    # all-to-all: rank c receives chunk c from every rank
-    recv_c, recv_s = [None] * W, [None] * W
-    reqs = []
-    for c in range(W):
-        clo, chi, cb0, cb1 = chunks[c]
-        cc = codes[clo * BITS // 8: cb1 * BLOCK * BITS // 8]
-        cs = scales[cb0:cb1]
-        if c == rank:
-            recv_c[rank], recv_s[rank] = cc.copy(), cs.copy()
-            continue
-        reqs.append(dist.isend(torch.from_numpy(cc.copy()), dst=c))
-        reqs.append(dist.isend(torch.from_numpy(cs.view(np.int16).copy()), dst=c))
-    for w in range(W):
-        if w == rank:
-            continue
-        tc = torch.empty((b1 - b0) * BLOCK * BITS // 8, dtype=torch.uint8)
-        ts = torch.empty(b1 - b0, dtype=torch.int16)
-        dist.recv(tc, src=w)
-        dist.recv(ts, src=w)
-        recv_c[w], recv_s[w] = tc.numpy(), ts.numpy().view(np.uint16)
-    for r in reqs:
-        r.wait()
-    # local reduce + stage-2 requantisation of this rank's chunk
-    p2 = O.params(BITS, BLOCK, O.SR, seed=77, index_offset=step * N + lo, philox_stream=1)
-    _, co, so = O.unpack_dequant_reduce_requant(recv_c, recv_s, hi - lo, O.params(BITS, BLOCK),
-                                                False, e2_shard, p2)
-    gathered = [None] * W
-    dist.all_gather_object(gathered, (co, so, e2_shard.copy()))
-    if rank == 0:
-        np.savez(os.path.join(outdir, f"step{step}.npz"),
-                 codes=np.concatenate([x[0] for x in gathered]),
-                 scales=np.concatenate([x[1] for x in gathered]),
-                 e2=np.concatenate([x[2] for x in gathered]))
-
-
-def _simulate(O, W):
-    errs = [np.zeros(N, np.float32) for _ in range(W)]
-    e2 = np.zeros(N, np.float32)
-    outs = []
-    for step in range(STEPS):
-        enc = []
-        for w in range(W):
-            p1 = O.params(BITS, BLOCK, O.SR, seed=1000 + w, index_offset=step * N)
-            enc.append(O.quantize_pack(_grad(w, step), p1, errs[w]))
-        p2 = O.params(BITS, BLOCK, O.SR, seed=77, index_offset=step * N, philox_stream=1)
-        _, co, so = O.unpack_dequant_reduce_requant([c for c, _ in enc], [s for _, s in enc], N,
-                                                    O.params(BITS, BLOCK), False, e2, p2)
-        outs.append((co, so, e2.copy()))
-    return outs, errs
+def _run_ranks(W, tmp_path, drop=None, timeout_s=None, join_s=300):
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, W, port, str(tmp_path), drop, timeout_s)) for r in range(W)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=join_s)
+    return procs
 
 
 @pytest.mark.parametrize("W", [2, 3])
 def test_gloo_ranks_equal_single_process_simulation(orc, tmp_path, W):
-    torch = pytest.importorskip("torch")
-    import torch.multiprocessing as mp
-    ctx = mp.get_context("spawn")
-    port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, W, port, str(tmp_path))) for r in range(W)]
-    for p in procs:
-        p.start()
-    for p in procs:
-        p.join(timeout=300)
+    pytest.importorskip("torch")
+    import sharded_sim
+    procs = _run_ranks(W, tmp_path)
     assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
-    outs, errs = _simulate(orc, W)
+    grads = [[_grad(w, t) for w in range(W)] for t in range(STEPS)]
+    results, errs, e2 = sharded_sim.simulate(grads, N, BITS, BLOCK, 1, [1000 + w for w in range(W)], 77,
+                                             BUCKET_BYTES, mul=1.0 / W)
     for step in range(STEPS):
-        got = np.load(tmp_path / f"step{step}.npz")
-        co, so, e2 = outs[step]
-        assert got["codes"].tobytes() == co.tobytes()
-        assert np.array_equal(got["scales"], so)
-        assert np.array_equal(got["e2"].view(np.uint32), e2.view(np.uint32))
+        codes, scales, out = results[step]
+        for w in range(W):
+            got = np.load(tmp_path / f"step{step}_rank{w}.npz")
+            assert got["codes"].tobytes() == codes.tobytes(), (step, w)
+            assert np.array_equal(got["scales"], scales), (step, w)
+            assert np.array_equal(got["out"].view(np.uint32), out.view(np.uint32)), (step, w)
     for w in range(W):
         assert np.array_equal(np.load(tmp_path / f"err{w}.npy").view(np.uint32), errs[w].view(np.uint32))
-    del torch
+        shard = sharded_sim.shard_of(e2, N, W, w, BLOCK, BUCKET_BYTES)
+        assert np.array_equal(np.load(tmp_path / f"e2_{w}.npy").view(np.uint32), shard.view(np.uint32))
 
 
 def test_bench_reference_arm_under_torchrun(tmp_path):
@@ -187,16 +143,8 @@ def test_rank_that_leaves_is_detected_on_the_host(tmp_path):
     # record it and exit, instead of waiting for ever.
     pytest.importorskip("torch")
     import time
-    import torch.multiprocessing as mp
-    ctx = mp.get_context("spawn")
-    port = _free_port()
-    W = 2
-    procs = [ctx.Process(target=_worker, args=(r, W, port, str(tmp_path), (1, 1), 20)) for r in range(W)]
     t0 = time.monotonic()
-    for p in procs:
-        p.start()
-    for p in procs:
-        p.join(timeout=240)
+    procs = _run_ranks(2, tmp_path, drop=(1, 1), timeout_s=20, join_s=240)
     alive = [p.is_alive() for p in procs]
     for p in procs:
         if p.is_alive():
@@ -208,4 +156,64 @@ def test_rank_that_leaves_is_detected_on_the_host(tmp_path):
     step, what = failed.read_text().split("\n", 1)
     assert step == "1" and what.strip()
     # step 0 completed on both ranks before the drop
-    assert (tmp_path / "step0.npz").exists()
+    assert (tmp_path / "step0_rank0.npz").exists() and (tmp_path / "step0_rank1.npz").exists()
+
+
+BENCH_N, BENCH_BUCKET = 2 * 4096 + 256, 8 * 1024      # bf16: three buckets of 4096, 4096, 256
+
+
+def _bench_grad(rank):
+    import torch
+    return torch.from_numpy(_grad(rank, 0)[:BENCH_N].copy()).to(torch.bfloat16)
+
+
+def _bench_worker(rank, W, port, outdir):
+    """One rank of bench.py's multi-GPU mode (its setup, parameters and call),
+    with the oracle codec on host tensors in place of the GPU."""
+    import sys
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import torch
+    import torch.distributed as dist
+
+    import bench
+    import bit_gradient_communication_gb300 as bc
+    from bit_gradient_communication_gb300 import sharded, synth
+    from oracle_codec import OracleCodec
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=W)
+    ar, grad = bench.sharded_rank(torch, bc, synth, sharded, BENCH_N, rank, W, "cpu", BENCH_BUCKET,
+                                  codec=OracleCodec(), exchange=sharded.Exchange(), grad=_bench_grad(rank))
+    codes = torch.zeros(bc.packed_bytes(BENCH_N, 4, 128), dtype=torch.uint8)
+    scales = torch.zeros(bc.num_blocks(BENCH_N, 128), dtype=torch.int16)
+    ar.finish(ar.reduce(ar.send(grad)), out_codes=codes, out_scales=scales)
+    np.savez(os.path.join(outdir, f"bench{rank}.npz"), codes=codes.numpy(), scales=scales.numpy().view(np.uint16),
+             err=ar.err.numpy())
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_bench_multi_gpu_mode_is_the_simulated_all_reduce(orc, tmp_path):
+    torch = pytest.importorskip("torch")
+    import torch.multiprocessing as mp
+
+    import sharded_sim
+    W = 2
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_bench_worker, args=(r, W, port, str(tmp_path))) for r in range(W)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=300)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    grads = [[_bench_grad(w).view(torch.int16).numpy().view(np.uint16) for w in range(W)]]
+    results, errs, _ = sharded_sim.simulate(grads, BENCH_N, 4, 128, 0, [1000 + w for w in range(W)], 0,
+                                            BENCH_BUCKET, elem_bytes=2)
+    codes, scales, _ = results[0]
+    for w in range(W):
+        got = np.load(tmp_path / f"bench{w}.npz")
+        assert got["codes"].tobytes() == codes.tobytes()
+        assert np.array_equal(got["scales"], scales)
+        assert np.array_equal(got["err"].view(np.uint32), errs[w].view(np.uint32))
