@@ -277,6 +277,17 @@ __global__ void __launch_bounds__(kThreads16, 3) encode16_kernel(const EncArgs a
 #pragma unroll
             for (int j = 0; j < 8; ++j) stat = fmaxf(stat, fmaxf(fabsf(v0[j]), fabsf(v1[j])));
         }
+        // the packed form of stochastic rounding (codes only) tests its pieces
+        // for tiny elements here, while the block statistic is exchanged
+        constexpr bool kPacked = SR && !EF && !DEQ && (BITS == 2 || BITS == 4);
+        bool tiny0 = false, tiny1 = false;
+        if constexpr (kPacked) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                tiny0 |= fabsf(v0[j]) < 0x1p-96f;
+                tiny1 |= fabsf(v1[j]) < 0x1p-96f;
+            }
+        }
         stat = team_reduce<BITS == 1>(stat, team, red[parity]);
         const int64_t blk = e0 >> a.log2B;
         int n_valid = 1 << a.log2B;
@@ -298,8 +309,18 @@ __global__ void __launch_bounds__(kThreads16, 3) encode16_kernel(const EncArgs a
         }
         Packed<BITS> c0, c1;
         float q0[8], q1[8];
-        quantize8<BITS, SR>(v0, s, y, rw0, c0, q0);
-        quantize8<BITS, SR>(v1, s, y, rw1, c1, q1);
+        if constexpr (kPacked) {
+            if (s >= 0x1p-14f && s < 65504.0f) {      // a normal, unsaturated scale
+                quantize8_sr_packed<BITS>(v0, s, y, rw0, tiny0, a.pack_mul, c0);
+                quantize8_sr_packed<BITS>(v1, s, y, rw1, tiny1, a.pack_mul, c1);
+            } else {
+                quantize8<BITS, SR>(v0, s, y, rw0, c0, q0);
+                quantize8<BITS, SR>(v1, s, y, rw1, c1, q1);
+            }
+        } else {
+            quantize8<BITS, SR>(v0, s, y, rw0, c0, q0);
+            quantize8<BITS, SR>(v1, s, y, rw1, c1, q1);
+        }
         if (e0 < (a.nb << a.log2B)) {
             uint8_t* p = a.codes + e0 * BITS / 8;
             if constexpr (BITS == 1) {
@@ -367,7 +388,9 @@ static cudaError_t run_encode16(const EncArgs& a, cudaStream_t st)
         cap.store(c, std::memory_order_relaxed);
     }
     const int grid = (int)(rows < c ? rows : c);
-    encode16_kernel<IN, BITS, EF, SR, DEQ><<<grid, kThreads16, 0, st>>>(a);
+    EncArgs b = a;
+    b.pack_mul = BITS <= 8 ? (1u << BITS) : 0u;
+    encode16_kernel<IN, BITS, EF, SR, DEQ><<<grid, kThreads16, 0, st>>>(b);
     return cudaGetLastError();
 }
 

@@ -53,6 +53,7 @@ struct EncArgs {
     uint64_t index_offset;
     int hadamard;           // 0 or the transform block H
     float* deq = nullptr;   // fused roundtrip only: fl(s*q) as fp32 [n]
+    uint32_t pack_mul = 0;  // 2^bits, set by the launcher (packing by multiply-adds)
 };
 
 constexpr int kMaxRanks = 64;

@@ -117,15 +117,56 @@ def test_encoder_special_blocks():
     x[512] = -0.0
     x[640:768] = np.linspace(-3, 3, 128)
     for bits in BITS:
-        for ef in (False, True):
-            e = np.zeros(n, np.float32)
-            p = bc.QParams(bits, 128)
-            codes, scales, err = _run_encode(torch, bc, x, "f32", n, p, e.copy() if ef else None)
-            e_ref = e.copy() if ef else None
-            c_ref, s_ref = O.quantize_pack(x, O.params(bits, 128), e_ref)
-            assert codes.tobytes() == c_ref.tobytes() and np.array_equal(scales, s_ref)
-            if ef:
-                assert np.array_equal(err.view(np.uint32), e_ref.view(np.uint32))
+        for rounding in (bc.RTN, bc.SR):
+            for ef in (False, True):
+                e = np.zeros(n, np.float32)
+                p = bc.QParams(bits, 128, rounding, seed=3)
+                codes, scales, err = _run_encode(torch, bc, x, "f32", n, p, e.copy() if ef else None)
+                e_ref = e.copy() if ef else None
+                c_ref, s_ref = O.quantize_pack(x, O.params(bits, 128, rounding, seed=3), e_ref)
+                tag = f"bits={bits} rounding={rounding} ef={ef}"
+                assert codes.tobytes() == c_ref.tobytes() and np.array_equal(scales, s_ref), tag
+                if ef:
+                    assert np.array_equal(err.view(np.uint32), e_ref.view(np.uint32)), tag
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8, 12, 16])
+@pytest.mark.parametrize("block", [32, 128, 4096])
+def test_sr_codes_past_the_range_are_clamped(bits, block):
+    # Blocks whose scale rounds down by half an fp16 ulp (absmax / Qmax = 1 +
+    # 2^-11, a tie that goes to 1.0) give t = +-Qmax (1 + 2^-11) at the block
+    # maximum.  Placed where the element's u = (r mod 2^23) 2^-23 is within
+    # Qmax 2^-11 of 1 (for -absmax) or of 0 (for +absmax), stochastic rounding
+    # lands on -Qmax - 1 or Qmax + 1 before the clamp; the codes must be the
+    # oracle's (the clamped ones) with and without error feedback.
+    torch, bc = need_gpu()
+    Q = (1 << (bits - 1)) - 1
+    A = np.float32(Q * (1 + 2.0 ** -11))
+    assert np.float32(A / np.float32(Q)).astype(np.float16) == np.float16(1.0)
+    n, seed, off = 1 << 18, 21, 1 << 20
+    u = (O.random_words(seed, 0, off, n) & 0x7FFFFF).astype(np.float64) * 2.0 ** -23
+    rng = np.random.default_rng(bits + block)
+    x = rng.uniform(-A / 2, A / 2, n).astype(np.float32)
+    idx = np.arange(n)
+    low = np.nonzero((u >= 1 - Q * 2.0 ** -11) & (idx % 2 == 0))[0]      # disjoint sets (at 12 and 16
+    high = np.nonzero((u < Q * 2.0 ** -11) & (idx % 2 == 1))[0]           # bits every u qualifies)
+    x[low], x[high] = -A, A
+    # the unclamped stochastic rounding of the planted elements leaves the range
+    t = np.float64(np.float32(A)) / 1.0
+    assert (np.floor(-t) + (u[low] < -t - np.floor(-t)) < -Q).any()
+    assert (np.floor(t) + (u[high] < t - np.floor(t)) > Q).any()
+    p = bc.QParams(bits, block, bc.SR, seed=seed, index_offset=off)
+    for ef in (False, True):
+        e = np.zeros(n, np.float32)
+        codes, scales, err = _run_encode(torch, bc, x, "f32", n, p, e.copy() if ef else None)
+        e_ref = e.copy() if ef else None
+        c_ref, s_ref = O.quantize_pack(x, O.params(bits, block, O.SR, seed=seed, index_offset=off), e_ref)
+        assert np.array_equal(scales, s_ref)
+        assert codes.tobytes() == c_ref.tobytes(), f"ef={ef}"
+        if ef:
+            assert np.array_equal(err.view(np.uint32), e_ref.view(np.uint32))
+        q = codes_to_q(unpack_codes(codes, bits, n), bits)
+        assert q.min() == -Q and q.max() == Q
 
 
 def _zero_fraction_indices(seed, count=3):
@@ -239,6 +280,44 @@ def test_sr_takes_the_exact_fraction(bits):
         assert np.array_equal(e2_g.cpu().numpy().view(np.uint32), e2_ref.view(np.uint32))
         q = codes_to_q(unpack_codes(got, bits, n), bits)
         assert (q[sel2] == q2_exp).all(), f"W={W}"
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8, 16])
+def test_sr_philox_counter_carry(bits):
+    # Element indices around 2^34, where the Philox counter i/4 carries into its
+    # high word: the kernels share Philox products between consecutive counters
+    # only while the high word stays the same, and fall back at the carry.  The
+    # encoders (16 elements per thread without error feedback, 8 with it) and
+    # the stochastic requantisation of the decoders (W = 3 general, W = 8
+    # 4-bit 16-element layout) must give the oracle's bits on both sides.
+    torch, bc = need_gpu()
+    n, off = 8192, (1 << 34) - 4096 - 24
+    x, e = _inputs(n, "f32", 77 + bits)
+    for ef in (False, True):
+        p = bc.QParams(bits, 128, bc.SR, seed=99, index_offset=off)
+        codes, scales, err = _run_encode(torch, bc, x, "f32", n, p, e.copy() if ef else None)
+        e_ref = e.copy() if ef else None
+        c_ref, s_ref = O.quantize_pack(x, O.params(bits, 128, O.SR, seed=99, index_offset=off), e_ref)
+        assert codes.tobytes() == c_ref.tobytes() and np.array_equal(scales, s_ref), f"ef={ef}"
+        if ef:
+            assert np.array_equal(err.view(np.uint32), e_ref.view(np.uint32))
+    rng = np.random.default_rng(bits)
+    for W in (3, 8):
+        ins = [_random_codes(rng, n, bits, 128) for _ in range(W)]
+        e2 = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+        e2_g = torch.from_numpy(e2.copy()).cuda()
+        pout = bc.QParams(bits, 128, bc.SR, seed=5, index_offset=off, philox_stream=1)
+        co, so = bc.alloc_codes(n, pout)
+        bc.unpack_dequant_reduce_requant([torch.from_numpy(c).cuda() for c, _ in ins],
+                                         [torch.from_numpy(s.view(np.int16)).cuda() for _, s in ins], n,
+                                         bc.QParams(bits, 128), err2=e2_g, p_out=pout, codes_out=co, scales_out=so)
+        torch.cuda.synchronize()
+        _, c_ref, s_ref = O.unpack_dequant_reduce_requant(
+            [c for c, _ in ins], [s for _, s in ins], n, O.params(bits, 128), False, e2,
+            O.params(bits, 128, O.SR, seed=5, index_offset=off, philox_stream=1))
+        assert co.cpu().numpy().tobytes() == c_ref.tobytes(), f"W={W}"
+        assert np.array_equal(so.cpu().numpy().view(np.uint16), s_ref), f"W={W}"
+        assert np.array_equal(e2_g.cpu().numpy().view(np.uint32), e2.view(np.uint32)), f"W={W}"
 
 
 def _random_codes(rng, n, bits, block, scale_sigma=1e-3):
