@@ -257,21 +257,27 @@ def run_ours(args, rank, world, local_rank):
 
     # end to end: pinned host gradients -> device, the step, requantised result -> host
     e2e = run_e2e(torch, bc, ar, args, dev) if not args.no_e2e else None
+    n_chunks = len(ar.chunks)
     if world > 1:
         t = torch.tensor([e2e["step_ms"] if e2e else 0.0], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         if e2e:
             e2e["step_ms"] = float(t.item())
 
+    legs = None
+    if rank == 0 and world == 1 and not args.no_legs:
+        del ar
+        torch.cuda.empty_cache()
+        legs = target_legs(torch, bc, synth, args.leg_steps)
     if rank != 0:
         return
     elems = W * n * world
     value = elems * 4 / (step_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak_gbs()
     enc_launch_s = enc_ms / W * 1e-3
-    dec_launch_s = dec_ms / len(ar.chunks) * 1e-3
+    dec_launch_s = dec_ms / n_chunks * 1e-3
     enc_bytes = n * ENC_BYTES_PER_ELEM
-    dec_bytes = (n / len(ar.chunks)) * DEC_BYTES_PER_ELEM
+    dec_bytes = (n / n_chunks) * DEC_BYTES_PER_ELEM
     enc_gbs = enc_bytes / enc_launch_s / 1e9
     dec_gbs = dec_bytes / dec_launch_s / 1e9
     src = kernel_src_hash()
@@ -279,14 +285,14 @@ def run_ours(args, rank, world, local_rank):
     tr = NCU_TRAFFIC.get("encode")
     traffic = round(tr["bytes_per_elem"] * n) if tr and tr["src"] == tsrc else None
     trd = NCU_TRAFFIC.get("decode")
-    dec_traffic = round(trd["bytes_per_elem"] * n / len(ar.chunks)) if trd and trd["src"] == tsrc else None
+    dec_traffic = round(trd["bytes_per_elem"] * n / n_chunks) if trd and trd["src"] == tsrc else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "ranks_simulated": W, "elements_per_rank": n,
                    "input_dtype": "bf16", "bits": BITS, "block": BLOCK, "rounding": "rtn",
-                   "error_feedback": "stage1+stage2", "chunks": len(ar.chunks),
+                   "error_feedback": "stage1+stage2", "chunks": n_chunks,
                    "l2": "inputs larger than L2 (%.1f GB of gradients per step)" % (W * n * 2 / 1e9),
                    "input_gbs_bf16": round(W * n * 2 * world / (step_ms * 1e-3) / 1e9, 2),
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
@@ -302,11 +308,13 @@ def run_ours(args, rank, world, local_rank):
                           "launch_ms": round(dec_launch_s * 1e3, 4), "bytes_per_elem": DEC_BYTES_PER_ELEM,
                           "traffic": dec_traffic, "bytes_per_launch": dec_bytes},
         },
-        "gpu_launches": K * (W + len(ar.chunks)),
+        "gpu_launches": K * (W + n_chunks),
         "clocks": clk,
         "kernel_src": src,
         "traffic_src": tsrc,
     }
+    if legs:
+        line["kernels"].update(legs)
     if e2e:
         line["e2e"] = {"value": round(elems * 4 / (e2e["step_ms"] * 1e-3) / 1e9, 2), "unit": UNIT,
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
@@ -423,6 +431,64 @@ def run_sharded(args, rank, world, local_rank):
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                        "ms_per_step": round(e2e["step_ms"], 3)}
     print(json.dumps(line), flush=True)
+
+
+def target_legs(torch, bc, synth, K):
+    """Short timed legs for the other target points of the method's
+    measurement plan, each on its own full-size workload (inputs larger than
+    L2): device time per launch (CUDA events on the launching stream, launch
+    queued before the start event; see _timed), algorithmic bytes per launch,
+    GB/s and the fraction of the measured HBM copy bandwidth."""
+    peak, _ = measured_peak_gbs()
+    legs = {}
+
+    def leg(name, fn, nbytes, steps, note):
+        for _ in range(3):
+            fn()
+        ms = _timed(torch, fn, steps)
+        legs[name] = {"gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4),
+                      "launch_ms": round(ms, 4), "bytes_per_launch": nbytes, "workload": note}
+
+    wl = synth.WORKLOADS["sweep_laplace_256m"]
+    x = synth.gradients(wl.kind, wl.n, wl.seed, **wl.params)
+    deq = torch.empty(wl.n, device="cuda")
+    for rounding, tag in ((bc.RTN, "rtn"), (bc.SR, "sr")):
+        p = bc.QParams(4, 128, rounding, seed=wl.sr_seed)
+        codes, scales = bc.alloc_codes(wl.n, p)
+        note = f"268,435,456 fp32 Laplace(0, 1e-3), 4-bit, block 128, {tag}, no error feedback"
+        leg(f"sweep_b4_B128_{tag}_encode", lambda: bc.quantize_pack(x, p, None, codes, scales),
+            wl.n * (4 + 0.5 + 2 / 128), K, note)
+        if rounding == bc.RTN:
+            leg("sweep_b4_B128_decode_w1",
+                lambda: bc.unpack_dequant_reduce_requant([codes], [scales], wl.n, p, sum_out=deq),
+                wl.n * (0.5 + 2 / 128 + 4), K, note + "; W=1 decoder to fp32")
+        del codes, scales
+    del x, deq
+
+    wl = synth.WORKLOADS["allgather_decode_gpt1p3b"]
+    x = synth.gradients(wl.kind, wl.n, wl.seed, dtype=torch.bfloat16, **wl.params)
+    p = bc.QParams(wl.bits, wl.block)
+    codes, scales = bc.quantize_pack(x, p)
+    del x
+    out = torch.empty(wl.n, dtype=torch.bfloat16, device="cuda")
+    leg("allgather_decode_b4_B128_bf16", lambda: bc.unpack_dequant(codes, scales, wl.n, p, 1.0 / wl.ranks, out),
+        wl.n * (0.5 + 2 / 128 + 2), K, "1.3e9 4-bit block-128 codes to the bf16 mean of 8 ranks")
+    del codes, scales, out
+
+    wl = synth.WORKLOADS["gpt6p7b_2bit_buckets"]
+    x = synth.gradients(wl.kind, wl.n, wl.seed, dtype=torch.bfloat16, **wl.params)
+    err = torch.zeros(wl.n, device="cuda")
+    p = bc.QParams(wl.bits, wl.block, wl.rounding, seed=wl.sr_seed)
+    codes, scales = bc.alloc_codes(wl.n, p)
+    sched = bc.Scheduler(2, wl.bucket_bytes)
+    leg("gpt6p7b_2bit_buckets_encode", lambda: sched.quantize_pack(x, p, err, codes, scales),
+        wl.n * (2 + 8 + wl.bits / 8 + 2 / wl.block), max(3, K // 4),
+        "6.7e9 bf16 with 0.1% outliers, 2-bit block 64, stochastic rounding, error feedback, "
+        "512 buckets of 25 MiB on two streams (one step = all buckets)")
+    sched.close()
+    del x, err, codes, scales
+    torch.cuda.empty_cache()
+    return legs
 
 
 def run_e2e(torch, bc, ar, args, dev):
@@ -873,6 +939,8 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=1 << 21)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-legs", action="store_true", help="skip the target-point legs after the headline")
+    ap.add_argument("--leg-steps", type=int, default=20, help="timed launches per target-point leg")
     ap.add_argument("--sweep-filter", default=None,
                     help="bits,block,rtn|sr: run one configuration of sweep_laplace_256m")
     ap.add_argument("--workload", default=WORKLOAD,

@@ -10,8 +10,13 @@
 // framework's caching allocator, which may already hold all free memory).
 //
 // Limits and sharing rules (also stated in include/bitscom.h):
-//   * capacity: 8 MiB of codes + 1 MiB of scales, held by every GPU that loads
-//     the library until the process exits;
+//   * capacity: 8 MiB of codes + 1 MiB of scales per device.  The first call
+//     on a device looks the array's address up; with CUDA's lazy module
+//     loading that lookup loads this file's module, which reserves the array
+//     (and may synchronise the device), so callers make that call at set-up
+//     time.  The array stays until the process exits;
+//   * the address is cached per device number; after cudaDeviceReset the
+//     cached address is stale and calls on that device are not supported;
 //   * one array per device, shared by every call on that device: calls whose
 //     kernels overlap on the GPU (different streams, or different host threads
 //     without ordering) race on it;

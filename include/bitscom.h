@@ -211,15 +211,20 @@ bitscom_status bitscom_roundtrip(const void* x, bitscom_dtype dt, int64_t n, flo
  * gradient buffer and must not call the CUDA allocator, which can synchronise
  * the device and compete with a framework's caching allocator.  The codes and
  * scales live in a fixed device array of this library (8 MiB of codes + 1 MiB
- * of scales, held on every GPU that loads the library until exit); the caller
- * still passes x, err and deq_out as in bitscom_roundtrip, and the results are
- * identical to it.
+ * of scales per device); the caller still passes x, err and deq_out as in
+ * bitscom_roundtrip, and the results are identical to it.
  *   - n must not exceed bitscom_roundtrip_noalloc_max_elements(bits, block)
  *     (at least 4,194,304 for every bits/block; 16,777,216 for 4-bit, block
  *     128); larger n returns BITSCOM_EINVAL and enqueues nothing.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture on the device.
+ *     (cudaGetSymbolAddress) with that device current.  With CUDA's default
+ *     lazy module loading that lookup is what reserves the 9 MiB on the
+ *     device, and it may synchronise the device; it fails with BITSCOM_ECUDA
+ *     if the device has no 9 MiB left.  So make that first call at set-up
+ *     time, while memory is still free and before any stream capture on the
+ *     device.  The array then stays until the process exits.
+ *   - The address is kept per device number: after cudaDeviceReset (which
+ *     destroys the array) calls on that device are not supported.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents (nothing in it needs clearing: every code and scale is written
  *     before it is read).  Calls whose kernels overlap on the GPU race on it.

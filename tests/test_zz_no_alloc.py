@@ -36,13 +36,17 @@ def _abi_roundtrip(torch, bc, x, p, err, noalloc):
     return deq
 
 
-@pytest.mark.parametrize("dtype,bits,block,rounding,ef", [
-    ("f32", 4, 128, 0, False), ("bf16", 4, 128, 0, True), ("f32", 2, 64, 1, True),
-    ("f32", 1, 256, 0, True), ("bf16", 16, 8, 1, False), ("f32", 12, 4096, 0, True)])
-def test_noalloc_matches_roundtrip_twice(dtype, bits, block, rounding, ef):
+@pytest.mark.parametrize("dtype,bits,block,rounding,ef,hadamard", [
+    ("f32", 4, 128, 0, False, 0), ("bf16", 4, 128, 0, True, 0), ("f32", 2, 64, 1, True, 0),
+    ("f32", 1, 256, 0, True, 0), ("bf16", 16, 8, 1, False, 0), ("f32", 12, 4096, 0, True, 0),
+    ("f32", 4, 128, 0, True, 128)])
+def test_noalloc_matches_roundtrip_twice(dtype, bits, block, rounding, ef, hadamard):
+    # hadamard: the rotated codec takes the two-kernel path (encoder, then the
+    # single-rank decoder) through the shared array
     torch, bc = need_gpu()
-    p = bc.QParams(bits, block, rounding, seed=17)
-    for call, n in enumerate([3 * 4096 + 11, 5 * 4096]):
+    p = bc.QParams(bits, block, rounding, seed=17, hadamard=hadamard)
+    sizes = [3 * 4096, 5 * 4096] if hadamard else [3 * 4096 + 11, 5 * 4096]
+    for call, n in enumerate(sizes):
         g = torch.Generator(device="cuda").manual_seed(100 + call)
         x = torch.randn(n, generator=g, device="cuda") * 1e-3
         if dtype == "bf16":
@@ -77,3 +81,32 @@ def test_noalloc_rejects_sizes_beyond_its_capacity():
     torch.cuda.synchronize()
     assert torch.equal(got.view(torch.int32), ref.view(torch.int32))
     assert np.isfinite(got.cpu().numpy()).all()
+
+
+def test_noalloc_call_allocates_nothing():
+    # The point of the entry point: once the array is in place (a first call at
+    # set-up) and the caller's own buffers exist, a call allocates no device
+    # memory -- neither through torch's caching allocator nor outside it
+    # (cudaMemGetInfo's free bytes are the same before and after, at points
+    # where the device is idle).
+    torch, bc = need_gpu()
+    L = bc.lib()
+    n = 5 * 4096 + 3
+    p = bc.QParams(4, 128, bc.SR, seed=3)
+    x = torch.randn(n, device="cuda")
+    err = torch.zeros(n, device="cuda")
+    deq = torch.empty(n, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        st = L.bitscom_roundtrip_noalloc(x.data_ptr(), bc.F32, n, err.data_ptr(), ctypes.byref(p.c()),
+                                         deq.data_ptr(), stream)
+        assert st == 0, bc.STATUS.get(st, st)
+
+    call()                                   # set-up: the array's address, the kernels' modules
+    torch.cuda.synchronize()
+    before = (torch.cuda.memory_allocated(), torch.cuda.memory_reserved(), torch.cuda.mem_get_info()[0])
+    call()
+    torch.cuda.synchronize()
+    after = (torch.cuda.memory_allocated(), torch.cuda.memory_reserved(), torch.cuda.mem_get_info()[0])
+    assert after == before
