@@ -14,6 +14,8 @@ Parity status of each function (details in the tests):
                                          telescoping error-feedback bound)
   unpack_dequant, f32_to_bf16            pinned (W=1 decoder sums, torch bf16 cast)
   fwht (Hadamard smoothing)              pinned (scipy Sylvester matrix, involution)
+  sum_ranks (full-precision local reduce) pinned (hand-worked order and -0 cases,
+                                         exact sums of small integers)
   qwd_encode, qwd_apply                  pinned (hand block, bound, telescoping)
   tail blocks (n mod B != 0), 1-bit SR   pinned to their readings (hand-worked
                                          tails, tail == zero-padded block,
@@ -105,6 +107,8 @@ def lib():
             L.orc_qwd_encode.argtypes = [vp, i32, i64, vp, P, vp, vp]
             L.orc_qwd_apply.restype = ctypes.c_int
             L.orc_qwd_apply.argtypes = [vp, vp, i64, P, vp, vp, i32]
+            L.orc_sum_ranks.restype = ctypes.c_int
+            L.orc_sum_ranks.argtypes = [vp, i32, i32, i64, vp]
             L.orc_fwht.restype = ctypes.c_int
             L.orc_fwht.argtypes = [vp, i64, i32]
             L.orc_num_blocks.restype = i64
@@ -249,6 +253,17 @@ def qwd_apply(codes, scales, n: int, p: Params, ref: np.ndarray, w_dtype=None):
     scales = np.ascontiguousarray(scales, dtype=np.uint16)
     if lib().orc_qwd_apply(_ptr(codes), _ptr(scales), n, ctypes.byref(p), _ptr(ref), _ptr(out),
                            0 if w_dtype in (None, F32) else 1):
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def sum_ranks(xs) -> np.ndarray:
+    """Rank-ordered fp32 sum of W arrays (float32, or uint16 bf16 bits)."""
+    xs = [np.ascontiguousarray(x) for x in xs]
+    n, W = xs[0].size, len(xs)
+    ptrs = (ctypes.c_void_p * W)(*[x.ctypes.data for x in xs])
+    out = np.zeros(n, dtype=np.float32)
+    if lib().orc_sum_ranks(ctypes.cast(ptrs, ctypes.c_void_p), _dtype_code(xs[0]), W, n, _ptr(out)):
         raise ValueError("oracle rejected the arguments")
     return out
 

@@ -419,6 +419,26 @@ int orc_unpack_dequant_reduce_requant(const uint8_t* const* codes_in,
     return 0;
 }
 
+/* Full-precision local reduce of the hierarchical all-reduce (bitscom README,
+ * "Implemented Features": pipeline-A local reduce; "Hierarchical All-Reduce
+ * Options": local_quantize=False keeps the local stage in full precision).
+ * Reading: the W local ranks' values are summed in fp32 in rank order, rank
+ * 0's value first: out = fl(...fl(x_0 + x_1)... + x_{W-1}); bf16 inputs are
+ * widened exactly. */
+int orc_sum_ranks(const void* const* x, int32_t dtype, int32_t W, int64_t n, float* out)
+{
+    if (!x || !out || W < 1 || n < 0 || (dtype != 0 && dtype != 1)) return 1;
+    for (int64_t i = 0; i < n; ++i) {
+        float s = 0.0f;
+        for (int32_t w = 0; w < W; ++w) {
+            float v = (dtype == 0) ? ((const float*)x[w])[i] : orc_bf16_to_f32(((const uint16_t*)x[w])[i]);
+            s = (w == 0) ? v : s + v;
+        }
+        out[i] = s;
+    }
+    return 0;
+}
+
 /* The all-gather side of the low-bit all-reduce: after the all-gather every
  * rank holds the requantised chunks of all ranks (bitscom README,
  * "Implemented Features": all-to-all -> local reduce -> all-gather) and

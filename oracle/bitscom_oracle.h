@@ -86,6 +86,11 @@ int orc_unpack_dequant(const uint8_t* codes, const uint16_t* scales, int64_t n,
                        const orc_params* p, float mul, int32_t out_dtype, void* out);
 uint16_t orc_f32_to_bf16(float x);
 
+/* Full-precision local reduce: out[i] = fl(...fl(x_0[i] + x_1[i])... +
+ * x_{W-1}[i]) in fp32, rank order, rank 0's value first (dtype 0 = fp32,
+ * 1 = bf16 bits). */
+int orc_sum_ranks(const void* const* x, int32_t dtype, int32_t W, int64_t n, float* out);
+
 /* Weight-difference quantisation for the sharded weight all-gather.
  * Sender: d = fl(w - ref) quantised (codes, scales); ref = fl(ref + fl(s*q)).
  * Receiver (every rank, on the gathered codes): ref = fl(ref + fl(s*q)), and

@@ -43,6 +43,9 @@ MUTANTS = {
     "encoder_skips_rotation": ("if (p->hadamard) orc_fwht(v, n, p->hadamard);", ";"),
     "qwd_reference_not_advanced": ("return orc_qwd_apply(codes, scales, n, p, ref, NULL, 0);", "return 0;"),
     "qwd_difference_sign": ("d[i] = wi - ref[i];", "d[i] = ref[i] - wi;"),
+    "local_sum_seeded_with_zero": ("s = (w == 0) ? v : s + v;", "s = s + v;"),
+    "local_sum_reverse_order": ("for (int32_t w = 0; w < W; ++w) {\n            float v = (dtype == 0) ? ((const float*)x[w])[i]",
+                                "for (int32_t w = W - 1; w >= 0; --w) {\n            float v = (dtype == 0) ? ((const float*)x[w])[i]"),
     "fma_in_feedback": ("float d = s * (float)q;          /* separate roundings, no FMA */\n                err_out[e] = val - d;",
                         "err_out[e] = fmaf(-s, (float)q, val);"),
 }

@@ -743,3 +743,35 @@ def test_qwd_receivers_track_the_sender(orc):
         torch = pytest.importorskip("torch")
         exp = torch.from_numpy(ref_recv.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
         np.testing.assert_array_equal(wout, exp)
+
+
+def test_sum_ranks_order_and_zeros(orc):
+    # The full-precision local reduce adds the ranks in order, rank 0 first, in
+    # fp32.  Worked by hand: 2^24 + 1 is a tie between 2^24 and 2^24 + 2 that
+    # goes to the even 2^24, so ((2^24 + 1) + 1) - 2^24 = 0 in rank order,
+    # while any order that adds the two ones first gives 2; and (-2^24 + 2^24)
+    # + 1 = 1 where ((1 + 2^24) - 2^24) would give 0.  Rank 0's -0 stays -0
+    # (a sum seeded with +0 would turn it into +0); +0 + -0 = +0.
+    big = np.float32(2.0 ** 24)
+    xs = [np.array([big, -big, 1.0, -0.0, 0.0], np.float32),
+          np.array([1.0, big, big, -0.0, -0.0], np.float32),
+          np.array([1.0, 1.0, -big, -0.0, -0.0], np.float32),
+          np.array([-big, 0.0, 0.0, -0.0, -0.0], np.float32)]
+    out = orc.sum_ranks(xs)
+    assert out.tolist()[:3] == [0.0, 1.0, 0.0]
+    assert np.signbit(out[3]) and not np.signbit(out[4])
+    # reversing the rank order changes both sums: (((-2^24 + 1) + 1) + 2^24) = 2
+    # exactly, and (0 + 1) + 2^24 is the tie that goes to 2^24, leaving 0
+    rev = orc.sum_ranks(xs[::-1])
+    assert rev.tolist()[:2] == [2.0, 0.0]
+
+
+def test_sum_ranks_exact_on_small_integers_and_bf16(orc):
+    # Sums of small integers are exact in any order: the closed form is the
+    # integer sum.  bf16 inputs widen exactly (bf16 bits << 16); integers up to
+    # 256 in magnitude are exact in bf16's 8 significant bits.
+    rng = np.random.default_rng(3)
+    xs = [rng.integers(-256, 257, 257).astype(np.float32) for _ in range(9)]
+    assert np.array_equal(orc.sum_ranks(xs), np.sum(np.array(xs, np.int64), axis=0).astype(np.float32))
+    bf = [(x.view(np.uint32) >> 16).astype(np.uint16) for x in xs]
+    assert np.array_equal(orc.sum_ranks(bf), orc.sum_ranks(xs))
