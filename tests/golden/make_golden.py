@@ -29,6 +29,43 @@ def bf16_bits(x):
     return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
 
 
+def exact_fraction_case():
+    """Stochastic rounding at the exact fraction: 2-bit codes, blocks of 8 with
+    scale 1 (each holds a 1.0).  Where an element's u = (r mod 2^23) 2^-23 lies in
+    (1/2, 3/4), its value is t = u - 1 + d for d = 2^-25, 0, -2^-25 in turn:
+    the fraction t - floor(t) = 1 + t is u + 2^-25, u, u - 2^-25, so q = 0, -1, -1
+    (rounding 1 + t to fp32 would give a tie that goes to u itself for d = 2^-25,
+    and q = -1).  expect_q lists those positions and their q."""
+    seed, n = 5, 1024
+    words = O.random_words(seed, 0, 0, n)
+    m = words & 0x7FFFFF
+    x = np.zeros(n, np.float32)
+    expect = []
+    used = set()
+    for h in np.nonzero((m > 1 << 22) & (m < 3 << 21))[0]:
+        h = int(h)
+        b0 = h // 8 * 8
+        if b0 in used:
+            continue
+        used.add(b0)
+        d = (2.0 ** -25, 0.0, -2.0 ** -25)[len(expect) % 3]
+        t = float(m[h]) * 2.0 ** -23 + d - 1.0
+        assert float(np.float32(t)) == t
+        x[b0 + (h - b0 + 4) % 8] = 1.0
+        x[h] = t
+        expect.append((h, 0 if d > 0 else -1))
+        if len(expect) == 9:
+            break
+    p = O.params(2, 8, O.SR, seed=seed)
+    codes, scales = O.quantize_pack(x, p)
+    mean = O.unpack_dequant(codes, scales, n, p, 0.5, O.BF16)
+    return {"bits": 2, "block": 8, "rounding": 1, "ef": False, "hadamard": 0, "n": n, "dtype": "f32",
+            "seed": seed, "index_offset": 0, "x": x.tobytes().hex(),
+            "err_in": np.zeros(n, np.float32).tobytes().hex(), "codes": codes.tobytes().hex(),
+            "scales": scales.tobytes().hex(), "err_out": None, "mean_bf16": mean.tobytes().hex(),
+            "expect_q": expect}
+
+
 def main():
     out = []
     for k, (bits, block, rnd, ef, H, n, dt) in enumerate(CASES):
@@ -46,6 +83,7 @@ def main():
                     "codes": codes.tobytes().hex(), "scales": scales.tobytes().hex(),
                     "err_out": e_out.tobytes().hex() if ef else None,
                     "mean_bf16": mean.tobytes().hex()})
+    out.append(exact_fraction_case())
     # a W=3 decoder case on the first three encodings' formats (4-bit, block 128)
     rng = np.random.default_rng(7)
     n = 384

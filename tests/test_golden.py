@@ -35,6 +35,20 @@ def test_oracle_reproduces_golden_encoder(orc, k):
     assert orc.unpack_dequant(codes, scales, c["n"], p, 0.5, orc.BF16).tobytes().hex() == c["mean_bf16"]
 
 
+def test_golden_exact_fraction_case_hits_the_tie():
+    # the stochastic-rounding case built at the exact fraction: the stored codes
+    # give the q the construction fixes (q = 0 where 1 + t rounded to fp32
+    # would have given -1)
+    from codec_util import codes_to_q, unpack_codes
+    cases = [c for c in GOLD["encoder"] if c.get("expect_q")]
+    assert len(cases) == 1
+    c = cases[0]
+    q = codes_to_q(unpack_codes(_arr(c["codes"], np.uint8), c["bits"], c["n"]), c["bits"])
+    assert len(c["expect_q"]) == 9
+    for pos, q_expected in c["expect_q"]:
+        assert q[pos] == q_expected, pos
+
+
 def test_oracle_reproduces_golden_decoder(orc):
     d = GOLD["decoder"]
     e2 = _arr(d["err2_in"], np.float32)
