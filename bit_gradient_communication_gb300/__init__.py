@@ -15,6 +15,7 @@ The names follow the C ABI:
   qwd_encode, qwd_apply          weight-difference quantisation (sharded
                                  weight all-gather)
   roundtrip                      quantise then dequantise
+  sum_ranks                      rank-ordered fp32 sum (full-precision local reduce)
   Scheduler                      fusion buckets on CUDA streams
 """
 from __future__ import annotations
@@ -105,6 +106,8 @@ def lib():
             L.bitscom_roundtrip.argtypes = [vp, st, i64, vp, P, vp, vp, vp, vp]
             L.bitscom_unpack_dequant.restype = st
             L.bitscom_unpack_dequant.argtypes = [vp, vp, i64, P, ctypes.c_float, st, vp, vp]
+            L.bitscom_sum_ranks.restype = st
+            L.bitscom_sum_ranks.argtypes = [vp, st, i32, i64, vp, vp]
             L.bitscom_qwd_encode.restype = st
             L.bitscom_qwd_encode.argtypes = [vp, st, i64, vp, P, vp, vp, vp]
             L.bitscom_qwd_apply.restype = st
@@ -247,6 +250,22 @@ def unpack_dequant(codes, scales, n: int, p: QParams, mul: float = 1.0, out=None
     _check(lib().bitscom_unpack_dequant(_dev_ptr(codes, "codes"), _dev_ptr(scales, "scales"), n,
                                         ctypes.byref(p.c()), ctypes.c_float(mul), _dtype_code(out),
                                         _dev_ptr(out, "out"), _stream(stream)), "bitscom_unpack_dequant")
+    return out
+
+
+def sum_ranks(xs: Sequence, out=None, stream=None):
+    """Rank-ordered fp32 sum of W = len(xs) fp32 or bf16 tensors of one size:
+    out = fl(...fl(x_0 + x_1)... + x_{W-1}).  Returns out (allocated when None)."""
+    torch = _torch()
+    W = len(xs)
+    n = xs[0].numel()
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=xs[0].device)
+    if any(x.numel() != n or x.dtype != xs[0].dtype for x in xs) or out.numel() != n:
+        raise ValueError("sum_ranks: every input and the output need the same size, inputs one dtype")
+    xp = (ctypes.c_void_p * W)(*[_dev_ptr(x, "x") for x in xs])
+    _check(lib().bitscom_sum_ranks(ctypes.cast(xp, ctypes.c_void_p), _dtype_code(xs[0]), W, n,
+                                   _dev_ptr(out, "out"), _stream(stream)), "bitscom_sum_ranks")
     return out
 
 

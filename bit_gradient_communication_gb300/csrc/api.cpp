@@ -236,6 +236,25 @@ bitscom_status bitscom_unpack_dequant(const void* codes, const uint16_t* scales,
                                                static_cast<cudaStream_t>(cuda_stream)));
 }
 
+bitscom_status bitscom_sum_ranks(const void* const* x, bitscom_dtype dt, int32_t W, int64_t n, float* out,
+                                 void* cuda_stream)
+{
+    if (W < 1 || W > bitscom::kMaxRanks || n < 0 || (dt != BITSCOM_F32 && dt != BITSCOM_BF16)) return BITSCOM_EINVAL;
+    if (n == 0) return BITSCOM_OK;
+    if (!x || !out) return BITSCOM_EINVAL;
+    bitscom::SumArgs a;
+    for (int w = 0; w < W; ++w) {
+        if (!x[w]) return BITSCOM_EINVAL;
+        if (!aligned(x[w], dt == BITSCOM_F32 ? 32 : 16)) return BITSCOM_EALIGN;
+        a.x[w] = x[w];
+    }
+    if (!aligned(out, 32)) return BITSCOM_EALIGN;
+    a.W = W;
+    a.n = n;
+    a.out = out;
+    return cuda_status(bitscom::launch_sum_ranks(a, dt == BITSCOM_F32 ? 0 : 1, static_cast<cudaStream_t>(cuda_stream)));
+}
+
 bitscom_status bitscom_qwd_encode(const void* w, bitscom_dtype dt, int64_t n, float* ref,
                                   const bitscom_qparams* p, void* codes_out, uint16_t* scales_out,
                                   void* cuda_stream)

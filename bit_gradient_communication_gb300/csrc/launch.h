@@ -84,6 +84,16 @@ struct DqArgs {
     int hadamard;           // 0 or the transform block H (inverse applied)
 };
 
+struct SumArgs {
+    const void* x[kMaxRanks];   // W arrays of n fp32 or bf16 elements
+    int W;
+    int64_t n;
+    float* out;                 // [n]
+};
+
+// Rank-ordered fp32 sum; dtype 0 = fp32, 1 = bf16 inputs.
+cudaError_t launch_sum_ranks(const SumArgs& a, int dtype, cudaStream_t st);
+
 // Return cudaErrorNotSupported for a combination without a kernel.
 cudaError_t launch_encode_f32(const EncArgs& a, int bits, bool sr, cudaStream_t st);
 cudaError_t launch_encode_bf16(const EncArgs& a, int bits, bool sr, cudaStream_t st);

@@ -1,0 +1,100 @@
+// sum_ranks.cu -- rank-ordered fp32 sum of W full-precision arrays: the local
+// reduce of the hierarchical all-reduce when local communication is not
+// quantised (bitscom README, "Implemented Features": hierarchical pipeline-A,
+// local reduce -> inter low-bit all-reduce -> local broadcast; "Hierarchical
+// All-Reduce Options": local_quantize=False keeps the local stage in full
+// precision).  out[i] = fl(...fl(fl(x_0[i]) + x_1[i])... + x_{W-1}[i]), the
+// ranks in order, so every implementation gets the same bits (a collective's
+// own reduction order is unspecified).
+//
+// HBM-bound streaming kernel: a persistent grid walks 8-element pieces; a
+// thread loads its piece of every rank (256-bit loads for fp32, 128-bit for
+// bf16, all in flight before the first add) and writes one 256-bit store.
+#include "codec.cuh"
+#include "launch.h"
+
+namespace bitscom {
+
+constexpr int kSumThreads = 256;
+
+template <int IN>
+__global__ void __launch_bounds__(kSumThreads) sum_ranks_kernel(const SumArgs a)
+{
+    const int64_t n = a.n;
+    const int64_t pieces = (n + 7) >> 3;
+    const int W = a.W;
+    for (int64_t pc = (int64_t)blockIdx.x * kSumThreads + threadIdx.x; pc < pieces;
+         pc += (int64_t)gridDim.x * kSumThreads) {
+        const int64_t e0 = pc << 3;
+        float r[8];
+        if (e0 + 8 <= n) {
+            // four ranks' loads in flight, then their adds in rank order (rank 0
+            // sets the sum)
+            for (int w0 = 0; w0 < W; w0 += 4) {
+                float v[4][8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (w0 + k >= W) break;
+                    if constexpr (IN == 0) {
+                        ld8_f32_stream(static_cast<const float*>(a.x[w0 + k]) + e0, v[k]);
+                    } else {
+                        bf16x8_to_f32(ld16_stream(static_cast<const uint16_t*>(a.x[w0 + k]) + e0), v[k]);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (w0 + k >= W) break;
+                    if (w0 + k == 0) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) r[j] = v[k][j];
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) r[j] = __fadd_rn(r[j], v[k][j]);
+                    }
+                }
+            }
+            st8_f32(a.out + e0, r);
+        } else {
+            for (int64_t i = e0; i < n; ++i) {
+                float s = 0.0f;
+                for (int w = 0; w < W; ++w) {
+                    float v;
+                    if constexpr (IN == 0) {
+                        v = static_cast<const float*>(a.x[w])[i];
+                    } else {
+                        v = __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x[w])[i] << 16);
+                    }
+                    s = w == 0 ? v : __fadd_rn(s, v);
+                }
+                a.out[i] = s;
+            }
+        }
+    }
+}
+
+template <int IN>
+static cudaError_t run_sum(const SumArgs& a, cudaStream_t st)
+{
+    static std::atomic<int> cap{0};
+    int c = cap.load(std::memory_order_relaxed);
+    if (c == 0) {
+        int dev = 0, occ = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sum_ranks_kernel<IN>, kSumThreads, 0);
+        c = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
+        cap.store(c, std::memory_order_relaxed);
+    }
+    const int64_t pieces = (a.n + 7) >> 3;
+    const int64_t blocks = (pieces + kSumThreads - 1) / kSumThreads;
+    const int grid = (int)(blocks < c ? blocks : c);
+    sum_ranks_kernel<IN><<<grid, kSumThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sum_ranks(const SumArgs& a, int dtype, cudaStream_t st)
+{
+    return dtype == 0 ? run_sum<0>(a, st) : run_sum<1>(a, st);
+}
+
+}  // namespace bitscom

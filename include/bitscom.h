@@ -172,6 +172,22 @@ bitscom_status bitscom_unpack_dequant(const void* codes, const uint16_t* scales,
                                       void* out, void* cuda_stream);
 
 /*
+ * Rank-ordered fp32 sum of W full-precision arrays: the local reduce of the
+ * hierarchical all-reduce when local communication is not quantised (bitscom
+ * README, "Implemented Features": hierarchical pipeline-A, local reduce ->
+ * inter low-bit all-reduce -> local broadcast; "Hierarchical All-Reduce
+ * Options": local_quantize=False, local full precision).
+ *   out[i] = fl(...fl(fl(x_0[i]) + x_1[i]) ... + x_{W-1}[i]): rank 0 sets the
+ *   sum (so -0 stays -0), the others are added in rank order in fp32 -- a
+ *   fixed order, unlike a collective's reduction.
+ *   x    host array of W device pointers (W in [1, 64]) to n elements each,
+ *        fp32 (32-byte aligned) or bf16 (16-byte aligned, converted exactly).
+ *   out  [n] fp32 (32-byte aligned); may not overlap any x[w].
+ */
+bitscom_status bitscom_sum_ranks(const void* const* x, bitscom_dtype dt, int32_t W, int64_t n, float* out,
+                                 void* cuda_stream);
+
+/*
  * Weight-difference quantisation for the sharded weight all-gather (SDP4Bit
  * README, "Weight Quantization Arguments": --quantized-weights,
  * --weight-quantization-bits 4, --wq-group-size 2048; "quantization on weight

@@ -96,7 +96,8 @@ def test_encoder_argument_checks(bc):
     assert call(x=0) == 1
     assert call(codes=0) == 1
     assert call(x=0x10010) == 2                           # fp32 x needs 32 bytes
-    assert call(dt=1, x=0x10010) != 2 or True
+    assert call(dt=1, x=0x10008) == 2                     # bf16 x needs 16 bytes
+    assert call(dt=1, x=0x10010, err=0x40010) == 2        # ... and error feedback 32 whatever x's type
     assert call(err=0x40004) == 2
     assert call(codes=0x20002) == 2                       # 4-bit codes need 4 bytes
     assert call(scales=0x30001) == 2
@@ -211,3 +212,17 @@ def test_qwd_argument_checks(bc):
     assert L.bitscom_qwd_apply(_fake(0x20000), _fake(0x30000), 4096, ctypes.byref(q), _fake(0x40004),
                                None, 0, None) == 2                  # reference alignment
     assert L.bitscom_qwd_apply(_fake(0x20000), _fake(0x30000), 0, ctypes.byref(q), None, None, 0, None) == 0
+
+
+def test_sum_ranks_argument_checks(bc):
+    L = bc.lib()
+    xs = (ctypes.c_void_p * 3)(0x10000, 0x20000, 0x30000)
+    call = lambda W=3, n=1024, dt=0, out=0x40000, x=xs: L.bitscom_sum_ranks(
+        ctypes.cast(x, ctypes.c_void_p) if x is not None else None, dt, W, n, _fake(out) if out else None, None)
+    assert call(n=0) == 0                                   # nothing enqueued
+    assert call(W=0) == 1 and call(W=65) == 1 and call(n=-1) == 1 and call(dt=2) == 1
+    assert call(out=0) == 1 and call(x=None) == 1
+    assert call(x=(ctypes.c_void_p * 3)(0x10000, 0, 0x30000)) == 1
+    assert call(x=(ctypes.c_void_p * 3)(0x10000, 0x20010, 0x30000)) == 2    # fp32 inputs need 32 bytes
+    assert call(dt=1, x=(ctypes.c_void_p * 3)(0x10000, 0x20008, 0x30000)) == 2  # bf16 inputs need 16
+    assert call(out=0x40010) == 2

@@ -734,3 +734,29 @@ def test_decoder_maximum_ranks(bits):
     assert co.cpu().numpy().tobytes() == c_ref.tobytes()
     assert np.array_equal(so.cpu().numpy().view(np.uint16), sc_ref)
     assert np.array_equal(e2g.cpu().numpy().view(np.uint32), e2_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("W", [1, 2, 3, 8, 64])
+def test_sum_ranks_matches_oracle(dt, W):
+    # The full-precision local reduce: rank-ordered fp32 sum, bit for bit,
+    # with values that tie (2^24 + 1) and zeros of both signs mixed in.
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(W * 7 + (dt == "bf16"))
+    for n in (1, 13, 8 * 4096 + 5):
+        xs = []
+        for w in range(W):
+            x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-3, 3)).astype(np.float32)
+            x[rng.integers(0, n, max(1, n // 50))] = np.float32(2.0 ** 24)
+            x[rng.integers(0, n, max(1, n // 50))] = 1.0
+            x[rng.integers(0, n, max(1, n // 50))] = -0.0
+            xs.append(x if dt == "f32" else bf16_bits_of(torch, x))
+        ref = O.sum_ranks(xs)
+        dev = [torch.from_numpy(x if dt == "f32" else x.view(np.int16)).cuda() for x in xs]
+        if dt == "bf16":
+            dev = [d.view(torch.bfloat16) for d in dev]
+        out = Guarded(torch, 4 * n)
+        bc.sum_ranks(dev, out=out.view(torch.float32))
+        torch.cuda.synchronize()
+        assert out.guards_intact()
+        assert np.array_equal(out.host(np.float32).view(np.uint32), ref.view(np.uint32)), f"n={n}"
