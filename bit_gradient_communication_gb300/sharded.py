@@ -119,6 +119,30 @@ class Exchange:
             return None
         return self.dist.all_gather_into_tensor(out, inp, group=self.group, async_op=True)
 
+    def _global(self, group_rank: int) -> int:
+        return group_rank if self.group is None else self.dist.get_global_rank(self.group, group_rank)
+
+    def gather(self, outs, inp, root: int = 0):
+        """The group's root receives every rank's inp into outs[rank] (a list of
+        equal-size tensors on the root, None elsewhere)."""
+        if self.host_staging:
+            h_outs = [o.cpu() for o in outs] if outs is not None else None
+            self.dist.gather(inp.cpu(), h_outs, dst=self._global(root), group=self.group)
+            if outs is not None:
+                for o, h in zip(outs, h_outs):
+                    o.copy_(h)
+            return None
+        return self.dist.gather(inp, outs, dst=self._global(root), group=self.group, async_op=True)
+
+    def broadcast(self, t, root: int = 0):
+        """t on every rank becomes the root's t."""
+        if self.host_staging:
+            h = t.cpu()
+            self.dist.broadcast(h, src=self._global(root), group=self.group)
+            t.copy_(h)
+            return None
+        return self.dist.broadcast(t, src=self._global(root), group=self.group, async_op=True)
+
 
 def _wait(handle):
     if handle is not None:
@@ -166,6 +190,7 @@ class LowBitAllReduce:
         b1, B1, b2, B2 = p1.bits, p1.block, p2.bits, p2.block
         mine = [bk.chunks[self.rank] for bk in self.buckets]
         self.shard = sum(hi - lo for lo, hi in mine)
+        self._e2_at = [sum(hi - lo for lo, hi in mine[:k]) for k in range(len(mine))]
         dev, u8 = self.device, torch.uint8
         f32 = torch.float32
         self.err = torch.zeros(n, dtype=f32, device=dev) if error_feedback else None
@@ -201,74 +226,97 @@ class LowBitAllReduce:
     def send(self, grad):
         """Steps 1 and 2: encode every bucket on the current stream; each
         bucket's all-to-all starts once it is encoded.  Returns the pending state."""
-        torch = self.torch
         if grad.numel() != self.n or grad.dtype != self.dtype:
             raise ValueError("gradient size or dtype differs from the one planned")
-        b1, B1 = self.p1.bits, self.p1.block
-        base = self.step * self.n
-        p1 = dataclasses.replace(self.p1, index_offset=self.p1.index_offset + base)
-        p2 = dataclasses.replace(self.p2, index_offset=self.p2.index_offset + base)
-        codes8, scales8 = self.codes, self.scales.view(torch.uint8)
-        a2a = []
-        for bk, buf in zip(self.buckets, self._bufs):
-            c0, c1 = bk.b0 * b1 // 8, bk.b0 * b1 // 8 + code_bytes(bk.b0, bk.b0 + bk.n, b1, B1)
-            s0, s1 = bk.b0 // B1, bk.b0 // B1 + scale_count(bk.b0, bk.b0 + bk.n, B1)
-            self.codec.quantize_pack(grad[bk.b0:bk.b0 + bk.n], p1.shifted(bk.b0),
-                                     None if self.err is None else self.err[bk.b0:bk.b0 + bk.n],
-                                     codes8[c0:c1], self.scales[s0:s1])
-            lo, hi = bk.chunks[self.rank]
-            in_c = [code_bytes(l, h, b1, B1) for l, h in bk.chunks]
-            in_s = [2 * scale_count(l, h, B1) for l, h in bk.chunks]
-            rc, rs = code_bytes(lo, hi, b1, B1), 2 * scale_count(lo, hi, B1)
-            a2a.append((self.ex.all_to_all(buf["rc"], codes8[c0:c1], [rc] * self.W, in_c),
-                        self.ex.all_to_all(buf["rs"], scales8[2 * s0:2 * s1], [rs] * self.W, in_s)))
-        self.step += 1
+        p1, p2 = self.begin_step()
+        a2a = [self.send_bucket(k, grad[bk.b0:bk.b0 + bk.n], p1) for k, bk in enumerate(self.buckets)]
         return {"p2": p2, "a2a": a2a}
 
     def reduce(self, state):
         """Steps 3 and 4: decode this rank's chunk of every bucket (rank-ordered
         sum, stage-2 error, requantisation); each chunk's all-gather starts once
         it is requantised."""
-        torch = self.torch
-        b1, B1, b2, B2 = self.p1.bits, self.p1.block, self.p2.bits, self.p2.block
-        p2 = state["p2"]
-        ag = []
-        e2_at = 0
-        for bk, buf, (h1, h2) in zip(self.buckets, self._bufs, state["a2a"]):
-            _wait(h1)
-            _wait(h2)
-            lo, hi = bk.chunks[self.rank]
-            nc = hi - lo
-            if nc > 0:
-                rc, rs = code_bytes(lo, hi, b1, B1), 2 * scale_count(lo, hi, B1)
-                cin = [buf["rc"][w * rc:(w + 1) * rc] for w in range(self.W)]
-                sin = [buf["rs"][w * rs:(w + 1) * rs].view(torch.int16) for w in range(self.W)]
-                oc, os_ = code_bytes(lo, hi, b2, B2), scale_count(lo, hi, B2)
-                self.codec.unpack_dequant_reduce_requant(
-                    cin, sin, nc, self.p1, sum_out=None,
-                    err2=None if self.err2 is None else self.err2[e2_at:e2_at + nc],
-                    p_out=p2.shifted(lo), codes_out=buf["sc"][:oc], scales_out=buf["ss"][:2 * os_].view(torch.int16))
-                e2_at += nc
-            ag.append((self.ex.all_gather(buf["gc"], buf["sc"]), self.ex.all_gather(buf["gs"], buf["ss"])))
-        return {"p2": p2, "ag": ag}
+        ag = [self.reduce_bucket(k, h, state["p2"]) for k, h in enumerate(state["a2a"])]
+        return {"p2": state["p2"], "ag": ag}
 
     def finish(self, state, out=None, mul: float = 1.0, out_codes=None, out_scales=None):
         """Step 5: every rank decodes the gathered codes of every bucket (and
         copies them to out_codes / out_scales when given)."""
-        torch = self.torch
-        b2, B2 = self.p2.bits, self.p2.block
-        for bk, buf, (h1, h2) in zip(self.buckets, self._bufs, state["ag"]):
-            _wait(h1)
-            _wait(h2)
-            nbytes = code_bytes(bk.b0, bk.b0 + bk.n, b2, B2)
-            nsc = scale_count(bk.b0, bk.b0 + bk.n, B2)
-            # pieces are padded to the largest chunk; only the last non-empty
-            # chunk is shorter, so the bucket's codes are the gathered prefix
-            gcodes, gscales = buf["gc"][:nbytes], buf["gs"][:2 * nsc].view(torch.int16)
-            if out_codes is not None:
-                out_codes[bk.b0 * b2 // 8: bk.b0 * b2 // 8 + nbytes].copy_(gcodes)
-            if out_scales is not None:
-                out_scales[bk.b0 // B2: bk.b0 // B2 + nsc].copy_(gscales)
-            if out is not None:
-                self.codec.unpack_dequant(gcodes, gscales, bk.n, state["p2"], mul, out[bk.b0:bk.b0 + bk.n])
+        for k, (bk, h) in enumerate(zip(self.buckets, state["ag"])):
+            self.finish_bucket(k, h, state["p2"], None if out is None else out[bk.b0:bk.b0 + bk.n], mul,
+                               out_codes, out_scales)
         return out
+
+    # -- one bucket at a time (the pipelined hierarchical all-reduce uses these) --
+    def begin_step(self):
+        """This step's stage parameters (Philox window step * n); advances the step."""
+        base = self.step * self.n
+        self.step += 1
+        return (dataclasses.replace(self.p1, index_offset=self.p1.index_offset + base),
+                dataclasses.replace(self.p2, index_offset=self.p2.index_offset + base))
+
+    def send_bucket(self, k: int, grad_bucket, p1):
+        """Encode bucket k (grad_bucket: its elements) and start its all-to-all."""
+        torch = self.torch
+        bk, buf = self.buckets[k], self._bufs[k]
+        b1, B1 = self.p1.bits, self.p1.block
+        c0, c1 = bk.b0 * b1 // 8, bk.b0 * b1 // 8 + code_bytes(bk.b0, bk.b0 + bk.n, b1, B1)
+        s0, s1 = bk.b0 // B1, bk.b0 // B1 + scale_count(bk.b0, bk.b0 + bk.n, B1)
+        self.codec.quantize_pack(grad_bucket, p1.shifted(bk.b0),
+                                 None if self.err is None else self.err[bk.b0:bk.b0 + bk.n],
+                                 self.codes[c0:c1], self.scales[s0:s1])
+        lo, hi = bk.chunks[self.rank]
+        in_c = [code_bytes(l, h, b1, B1) for l, h in bk.chunks]
+        in_s = [2 * scale_count(l, h, B1) for l, h in bk.chunks]
+        rc, rs = code_bytes(lo, hi, b1, B1), 2 * scale_count(lo, hi, B1)
+        scales8 = self.scales.view(torch.uint8)
+        return (self.ex.all_to_all(buf["rc"], self.codes[c0:c1], [rc] * self.W, in_c),
+                self.ex.all_to_all(buf["rs"], scales8[2 * s0:2 * s1], [rs] * self.W, in_s))
+
+    def reduce_bucket(self, k: int, a2a, p2):
+        """Decode this rank's chunk of bucket k once its all-to-all is done;
+        start the bucket's all-gather."""
+        torch = self.torch
+        bk, buf = self.buckets[k], self._bufs[k]
+        b1, B1, b2, B2 = self.p1.bits, self.p1.block, self.p2.bits, self.p2.block
+        _wait(a2a[0])
+        _wait(a2a[1])
+        lo, hi = bk.chunks[self.rank]
+        nc = hi - lo
+        if nc > 0:
+            rc, rs = code_bytes(lo, hi, b1, B1), 2 * scale_count(lo, hi, B1)
+            cin = [buf["rc"][w * rc:(w + 1) * rc] for w in range(self.W)]
+            sin = [buf["rs"][w * rs:(w + 1) * rs].view(torch.int16) for w in range(self.W)]
+            oc, os_ = code_bytes(lo, hi, b2, B2), scale_count(lo, hi, B2)
+            e2_at = self._e2_at[k]
+            self.codec.unpack_dequant_reduce_requant(
+                cin, sin, nc, self.p1, sum_out=None,
+                err2=None if self.err2 is None else self.err2[e2_at:e2_at + nc],
+                p_out=p2.shifted(lo), codes_out=buf["sc"][:oc], scales_out=buf["ss"][:2 * os_].view(torch.int16))
+        return self.ex.all_gather(buf["gc"], buf["sc"]), self.ex.all_gather(buf["gs"], buf["ss"])
+
+    def gathered(self, k: int, ag):
+        """Bucket k's requantised codes and scales once its all-gather is done.
+        The gathered pieces are padded to the largest chunk; only the last
+        non-empty chunk is shorter, so the bucket's codes are the prefix."""
+        torch = self.torch
+        bk, buf = self.buckets[k], self._bufs[k]
+        b2, B2 = self.p2.bits, self.p2.block
+        _wait(ag[0])
+        _wait(ag[1])
+        nbytes = code_bytes(bk.b0, bk.b0 + bk.n, b2, B2)
+        nsc = scale_count(bk.b0, bk.b0 + bk.n, B2)
+        return buf["gc"][:nbytes], buf["gs"][:2 * nsc].view(torch.int16)
+
+    def finish_bucket(self, k: int, ag, p2, out_bucket=None, mul: float = 1.0, out_codes=None, out_scales=None):
+        """Decode bucket k's gathered codes into out_bucket (its elements)."""
+        bk = self.buckets[k]
+        b2, B2 = self.p2.bits, self.p2.block
+        gcodes, gscales = self.gathered(k, ag)
+        if out_codes is not None:
+            out_codes[bk.b0 * b2 // 8: bk.b0 * b2 // 8 + gcodes.numel()].copy_(gcodes)
+        if out_scales is not None:
+            out_scales[bk.b0 // B2: bk.b0 // B2 + gscales.numel()].copy_(gscales)
+        if out_bucket is not None:
+            self.codec.unpack_dequant(gcodes, gscales, bk.n, p2, mul, out_bucket)
+        return out_bucket

@@ -48,3 +48,7 @@ class OracleCodec:
         dt = O.F32 if out.dtype == torch.float32 else O.BF16
         _np(out)[:] = O.unpack_dequant(codes.numpy(), _np(scales), n, params(p), mul, dt)
         return out
+
+    def sum_ranks(self, xs, out=None, stream=None):
+        out.numpy()[:] = O.sum_ranks([np.ascontiguousarray(_np(x)) for x in xs])
+        return out
