@@ -48,16 +48,18 @@ ENC_BYTES_PER_ELEM = 2 + 4 + 4 + BITS / 8 + 2 / BLOCK           # g bf16, e in, 
 DEC_BYTES_PER_ELEM = W_RANKS * (BITS / 8 + 2 / BLOCK) + 4 + 4 + BITS / 8 + 2 / BLOCK  # W inputs, e2 r/w, out
 
 # DRAM traffic per element measured by ncu (dram__bytes_read.sum +
-# dram__bytes_write.sum over the captured launch / its elements), valid only
-# while the sources of the two kernels' translation units (TRAFFIC_SOURCES)
-# hash to `src`.  Filled from profiles/.
+# dram__bytes_write.sum per launch / its elements), valid only while the
+# sources of the two kernels' translation units (TRAFFIC_SOURCES) hash to
+# `src`.  Captured on the same step with 2e8 elements per rank (each encoder
+# launch moves 2.1 GB, 16 times the L2), caches left alone between launches
+# (ncu --cache-control none), averaged over the step's 8 encoder and 8
+# decoder launches; the step's total equals its algorithmic bytes to 0.01 %,
+# and the full-size launches move the same bytes per element.
 TRAFFIC_SOURCES = ("launch.h", "codec.cuh", "encode_impl.cuh", "encode_bf16.cu", "decode_impl.cuh",
                    "decode_w8.cu")
 NCU_TRAFFIC = {
-    # profiles/launches_allreduce_w8_gpt1p3b.md: one full-size step, 1.3e9 elements per
-    # encoder launch, 1.625e8 output elements per decoder launch
-    "encode": {"src": "7824b74c713b748f", "bytes_per_elem": (7.800289e9 + 5.807496e9) / 1.3e9},
-    "decode": {"src": "7824b74c713b748f", "bytes_per_elem": (1.321248e9 + 0.6836018e9) / 1.625e8},
+    "encode": {"src": "cb1f53d0f4705fa7", "bytes_per_elem": 10.5090},
+    "decode": {"src": "cb1f53d0f4705fa7", "bytes_per_elem": 12.6893},
 }
 
 
