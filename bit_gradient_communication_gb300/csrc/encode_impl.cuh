@@ -301,8 +301,7 @@ __global__ void __launch_bounds__(kThreads16, 3) encode16_kernel(const EncArgs a
 
         uint32_t rw0[8], rw1[8];
         if constexpr (SR) {
-            random_words8(a.index_offset + (uint64_t)e0, a.keys, shift, rw0);
-            random_words8(a.index_offset + (uint64_t)e0 + 8, a.keys, shift, rw1);
+            random_words16(a.index_offset + (uint64_t)e0, a.keys, shift, rw0, rw1);
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) { rw0[j] = 0u; rw1[j] = 0u; }
