@@ -39,7 +39,12 @@ def _grad(rank, step):
     return synth.np_gradients("student_t3", N, 100 * rank + step, scale=1e-3)
 
 
-def _worker(rank, W, port, outdir, drop=None, timeout_s=None):
+# (bits1, block1, bits2, block2, hadamard): one format, and the two-level 8 -> 4-bit
+# format with Hadamard smoothing (chunks are then whole 512-element blocks)
+FORMATS = {"b4": (4, 128, 4, 128, 0), "tlq_hs": (8, 512, 4, 128, 128)}
+
+
+def _worker(rank, W, port, outdir, drop=None, timeout_s=None, fmt="b4"):
     """One rank.  drop = (rank, step): that rank leaves at the start of that
     step without a word (a crashed process); the others must notice on the
     host, through an error from the exchange, and leave that step cleanly."""
@@ -57,16 +62,17 @@ def _worker(rank, W, port, outdir, drop=None, timeout_s=None):
     os.environ["MASTER_PORT"] = str(port)
     kw = {"timeout": timedelta(seconds=timeout_s)} if timeout_s else {}
     dist.init_process_group("gloo", rank=rank, world_size=W, **kw)
-    ar = sharded.LowBitAllReduce(N, torch.float32, bc.QParams(BITS, BLOCK, bc.SR, seed=1000 + rank),
-                                 bc.QParams(BITS, BLOCK, bc.SR, seed=77, philox_stream=1), device="cpu",
+    b1, B1, b2, B2, H = FORMATS[fmt]
+    ar = sharded.LowBitAllReduce(N, torch.float32, bc.QParams(b1, B1, bc.SR, seed=1000 + rank, hadamard=H),
+                                 bc.QParams(b2, B2, bc.SR, seed=77, philox_stream=1, hadamard=H), device="cpu",
                                  bucket_bytes=BUCKET_BYTES, codec=OracleCodec(),
                                  exchange=sharded.Exchange(host_staging=(W == 3)))
     for step in range(STEPS):
         if drop is not None and drop == (rank, step):
             os._exit(0)
         g = torch.from_numpy(_grad(rank, step))
-        codes = torch.zeros(bc.packed_bytes(N, BITS, BLOCK), dtype=torch.uint8)
-        scales = torch.zeros(bc.num_blocks(N, BLOCK), dtype=torch.int16)
+        codes = torch.zeros(bc.packed_bytes(N, b2, B2), dtype=torch.uint8)
+        scales = torch.zeros(bc.num_blocks(N, B2), dtype=torch.int16)
         out = torch.empty(N)
         try:
             ar(g, out=out, mul=1.0 / W, out_codes=codes, out_scales=scales)
@@ -84,11 +90,11 @@ def _worker(rank, W, port, outdir, drop=None, timeout_s=None):
     dist.destroy_process_group()
 
 
-def _run_ranks(W, tmp_path, drop=None, timeout_s=None, join_s=300):
+def _run_ranks(W, tmp_path, drop=None, timeout_s=None, join_s=300, fmt="b4"):
     import torch.multiprocessing as mp
     ctx = mp.get_context("spawn")
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, W, port, str(tmp_path), drop, timeout_s)) for r in range(W)]
+    procs = [ctx.Process(target=_worker, args=(r, W, port, str(tmp_path), drop, timeout_s, fmt)) for r in range(W)]
     for p in procs:
         p.start()
     for p in procs:
@@ -96,15 +102,16 @@ def _run_ranks(W, tmp_path, drop=None, timeout_s=None, join_s=300):
     return procs
 
 
-@pytest.mark.parametrize("W", [2, 3])
-def test_gloo_ranks_equal_single_process_simulation(orc, tmp_path, W):
+@pytest.mark.parametrize("W,fmt", [(2, "b4"), (3, "b4"), (3, "tlq_hs")])
+def test_gloo_ranks_equal_single_process_simulation(orc, tmp_path, W, fmt):
     pytest.importorskip("torch")
     import sharded_sim
-    procs = _run_ranks(W, tmp_path)
+    procs = _run_ranks(W, tmp_path, fmt=fmt)
     assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
     grads = [[_grad(w, t) for w in range(W)] for t in range(STEPS)]
-    results, errs, e2 = sharded_sim.simulate(grads, N, BITS, BLOCK, 1, [1000 + w for w in range(W)], 77,
-                                             BUCKET_BYTES, mul=1.0 / W)
+    b1, B1, b2, B2, H = FORMATS[fmt]
+    results, errs, e2 = sharded_sim.simulate(grads, N, b1, B1, 1, [1000 + w for w in range(W)], 77,
+                                             BUCKET_BYTES, mul=1.0 / W, bits2=b2, block2=B2, hadamard=H)
     for step in range(STEPS):
         codes, scales, out = results[step]
         for w in range(W):
@@ -114,7 +121,7 @@ def test_gloo_ranks_equal_single_process_simulation(orc, tmp_path, W):
             assert np.array_equal(got["out"].view(np.uint32), out.view(np.uint32)), (step, w)
     for w in range(W):
         assert np.array_equal(np.load(tmp_path / f"err{w}.npy").view(np.uint32), errs[w].view(np.uint32))
-        shard = sharded_sim.shard_of(e2, N, W, w, BLOCK, BUCKET_BYTES)
+        shard = sharded_sim.shard_of(e2, N, W, w, B1, BUCKET_BYTES, block2=B2)
         assert np.array_equal(np.load(tmp_path / f"e2_{w}.npy").view(np.uint32), shard.view(np.uint32))
 
 

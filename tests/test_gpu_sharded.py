@@ -44,12 +44,18 @@ def _grad(torch, rank, step, bf16):
     return g.to(torch.bfloat16) if bf16 else g
 
 
-def _params(bc, rounding, rank):
-    return (bc.QParams(4, 128, rounding, seed=1000 + rank),
-            bc.QParams(4, 128, rounding, seed=77, philox_stream=1))
+# (bits1, block1, bits2, block2, hadamard): one format, and the two-level 8 -> 4-bit
+# format with Hadamard smoothing
+FORMATS = {"b4": (4, 128, 4, 128, 0), "tlq_hs": (8, 512, 4, 128, 128)}
 
 
-def _worker(rank, W, port, outdir, bf16, rounding):
+def _params(bc, rounding, rank, fmt, index_offset=0):
+    b1, B1, b2, B2, H = FORMATS[fmt]
+    return (bc.QParams(b1, B1, rounding, seed=1000 + rank, hadamard=H, index_offset=index_offset),
+            bc.QParams(b2, B2, rounding, seed=77, philox_stream=1, hadamard=H, index_offset=index_offset))
+
+
+def _worker(rank, W, port, outdir, bf16, rounding, fmt):
     import sys
     sys.path.insert(0, ROOT)
     import torch
@@ -63,13 +69,13 @@ def _worker(rank, W, port, outdir, bf16, rounding):
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=W)
     dt = torch.bfloat16 if bf16 else torch.float32
-    p1, p2 = _params(bc, rounding, rank)
+    p1, p2 = _params(bc, rounding, rank, fmt)
     ar = sharded.LowBitAllReduce(N, dt, p1, p2, device="cuda:0", bucket_bytes=BUCKET_BYTES,
                                  exchange=sharded.Exchange(host_staging=True))
     for step in range(STEPS):
         g = _grad(torch, rank, step, bf16).cuda()
-        codes = torch.zeros(bc.packed_bytes(N, 4, 128), dtype=torch.uint8, device="cuda")
-        scales = torch.zeros(bc.num_blocks(N, 128), dtype=torch.int16, device="cuda")
+        codes = torch.zeros(bc.packed_bytes(N, p2.bits, p2.block), dtype=torch.uint8, device="cuda")
+        scales = torch.zeros(bc.num_blocks(N, p2.block), dtype=torch.int16, device="cuda")
         out = torch.empty(N, device="cuda")
         ar(g, out=out, mul=1.0 / W, out_codes=codes, out_scales=scales)
         torch.cuda.synchronize()
@@ -81,15 +87,15 @@ def _worker(rank, W, port, outdir, bf16, rounding):
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("W,bf16,rounding", [(2, True, 0), (3, False, 1)])
-def test_ranks_on_libbitscom_equal_oracle_and_single_gpu_simulation(orc, tmp_path, W, bf16, rounding):
+@pytest.mark.parametrize("W,bf16,rounding,fmt", [(2, True, 0, "b4"), (3, False, 1, "b4"), (3, False, 1, "tlq_hs")])
+def test_ranks_on_libbitscom_equal_oracle_and_single_gpu_simulation(orc, tmp_path, W, bf16, rounding, fmt):
     torch, bc = need_gpu()
     import torch.multiprocessing as mp
 
     import sharded_sim
     ctx = mp.get_context("spawn")
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, W, port, str(tmp_path), bf16, rounding)) for r in range(W)]
+    procs = [ctx.Process(target=_worker, args=(r, W, port, str(tmp_path), bf16, rounding, fmt)) for r in range(W)]
     for p in procs:
         p.start()
     for p in procs:
@@ -102,8 +108,10 @@ def test_ranks_on_libbitscom_equal_oracle_and_single_gpu_simulation(orc, tmp_pat
     esz = 2 if bf16 else 4
     host = [[_grad(torch, w, t, bf16) for w in range(W)] for t in range(STEPS)]
     grads = [[(g.view(torch.int16).numpy().view(np.uint16) if bf16 else g.numpy()) for g in gw] for gw in host]
-    results, errs, e2 = sharded_sim.simulate(grads, N, 4, 128, rounding, [1000 + w for w in range(W)], 77,
-                                             BUCKET_BYTES, elem_bytes=esz, mul=1.0 / W)
+    b1, B1, b2, B2, H = FORMATS[fmt]
+    results, errs, e2 = sharded_sim.simulate(grads, N, b1, B1, rounding, [1000 + w for w in range(W)], 77,
+                                             BUCKET_BYTES, elem_bytes=esz, mul=1.0 / W, bits2=b2, block2=B2,
+                                             hadamard=H)
     # the library's single-GPU simulation of the same W ranks
     sched = bc.Scheduler(n_streams=2, bucket_bytes=BUCKET_BYTES)
     d_err = [torch.zeros(N, device="cuda") for _ in range(W)]
@@ -111,8 +119,8 @@ def test_ranks_on_libbitscom_equal_oracle_and_single_gpu_simulation(orc, tmp_pat
     sim = []
     for t in range(STEPS):
         xs = [g.cuda() for g in host[t]]
-        p1 = [bc.QParams(4, 128, rounding, seed=1000 + w, index_offset=t * N) for w in range(W)]
-        p2 = bc.QParams(4, 128, rounding, seed=77, philox_stream=1, index_offset=t * N)
+        p1 = [_params(bc, rounding, w, fmt, t * N)[0] for w in range(W)]
+        p2 = _params(bc, rounding, 0, fmt, t * N)[1]
         cs, ss = zip(*[bc.alloc_codes(N, p1[0]) for _ in range(W)])
         co, so = bc.alloc_codes(N, p2)
         sched.allreduce(xs, p1, cs, ss, d_err, p2, d_e2, co, so)
@@ -131,6 +139,6 @@ def test_ranks_on_libbitscom_equal_oracle_and_single_gpu_simulation(orc, tmp_pat
     for w in range(W):
         assert np.array_equal(np.load(tmp_path / f"err{w}.npy").view(np.uint32), errs[w].view(np.uint32))
         assert np.array_equal(d_err[w].cpu().numpy().view(np.uint32), errs[w].view(np.uint32))
-        shard = sharded_sim.shard_of(e2, N, W, w, 128, BUCKET_BYTES, elem_bytes=esz)
+        shard = sharded_sim.shard_of(e2, N, W, w, B1, BUCKET_BYTES, elem_bytes=esz, block2=B2)
         assert np.array_equal(np.load(tmp_path / f"e2_{w}.npy").view(np.uint32), shard.view(np.uint32))
     assert np.array_equal(d_e2.cpu().numpy().view(np.uint32), e2.view(np.uint32))
