@@ -185,12 +185,18 @@ class LowBitAllReduce:
         esz = torch.empty(0, dtype=dtype).element_size()
         if esz not in (2, 4):
             raise TypeError("gradients must be float32 or bfloat16")
+        if p1.hadamard != p2.hadamard:
+            raise ValueError("both stages of one all-reduce use the same Hadamard block (or none)")
         self.buckets = plan(n, esz, p1.block, p2.block, self.W, bucket_bytes)
         self.step = 0
         b1, B1, b2, B2 = p1.bits, p1.block, p2.bits, p2.block
-        mine = [bk.chunks[self.rank] for bk in self.buckets]
-        self.shard = sum(hi - lo for lo, hi in mine)
-        self._e2_at = [sum(hi - lo for lo, hi in mine[:k]) for k in range(len(mine))]
+        # this rank's stage-2 error shard: its chunk of every bucket, in bucket order
+        self._e2_at = []
+        self.shard = 0
+        for bk in self.buckets:
+            lo, hi = bk.chunks[self.rank]
+            self._e2_at.append(self.shard)
+            self.shard += hi - lo
         dev, u8 = self.device, torch.uint8
         f32 = torch.float32
         self.err = torch.zeros(n, dtype=f32, device=dev) if error_feedback else None
