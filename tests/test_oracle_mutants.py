@@ -27,6 +27,8 @@ MUTANTS = {
     "philox_multiplier": ("M0 = 0xD2511F53u", "M0 = 0xD2511F55u"),
     "philox_weyl": ("W1 = 0xBB67AE85u", "W1 = 0xBB67AE87u"),
     "sr_flipped": ("(double)f + (double)u < (double)t", "(double)f + (double)u > (double)t"),
+    "sr_uniform_from_high_bits": ("float u = (float)(r & 0x7FFFFFu) * (1.0f / 8388608.0f);",
+                                  "float u = (float)(r >> 8) * (1.0f / 16777216.0f);"),
     "sr_fraction_rounded": ("(double)f + (double)u < (double)t", "u < t - f"),
     "offset_off_by_one": ("return (uint32_t)(q + (1 << (bits - 1)));", "return (uint32_t)(q + (1 << (bits - 1)) - 1);"),
     "mean_over_block": ("x = sum / (float)n_valid;", "x = sum / (float)B;"),
