@@ -345,7 +345,11 @@ def run_sharded(args, rank, world, local_rank):
     """N > 1: every GPU is one rank of the low-bit all-reduce (W = N): encode
     its own gradient, all-to-all of the chunks over NCCL, decode-reduce-requant
     of its own chunk, all-gather of the requantised chunks.  value = all ranks'
-    gradient elements (counted as fp32 bytes) / the slowest rank's step time."""
+    gradient elements (counted as fp32 bytes) / the slowest rank's step time.
+    By default the gradient is one bucket, as in the single-GPU workload (one
+    encoder launch per rank, W chunks); --bucket-mb splits it into fusion
+    buckets whose exchange overlaps the next bucket's encoder (each bucket
+    costs a few Python-issued calls, so small buckets make the step host-bound)."""
     import torch
     import torch.distributed as dist
 
@@ -949,7 +953,9 @@ def main():
                     help="another workload recipe from synth.WORKLOADS (one JSON line of its own)")
     ap.add_argument("--replicas", action="store_true",
                     help="N > 1: run N independent copies of the single-GPU simulation instead of the sharded all-reduce")
-    ap.add_argument("--bucket-mb", type=int, default=25, help="N > 1: fusion bucket size in MiB of bf16 gradient")
+    ap.add_argument("--bucket-mb", type=int, default=0,
+                    help="N > 1: fusion bucket size in MiB of bf16 gradient (0: one bucket per rank, the workload's "
+                         "own structure: one encoder launch, W chunks)")
     ap.add_argument("--wl-n", type=int, default=0,
                     help="run --workload with this many elements instead (a small case for profilers)")
     args = ap.parse_args()
