@@ -1,5 +1,5 @@
-// Self-check of the codec's quotient v / s (div_by_scale: reciprocal + two
-// residual corrections) against CUDA's correctly rounded __fdiv_rn, for every
+// Self-check of the codec's quotient v / s (div_by_scale: reciprocal + one
+// residual correction) against CUDA's correctly rounded __fdiv_rn, for every
 // positive finite fp16 scale s and n_v values of v per scale: values whose
 // quotient lies within 4 ulps of a half-integer or an integer in
 // [-32768, 32768] (where rounding decisions are made), random quotients up to

@@ -1,6 +1,6 @@
 """The codec's divisions, checked on the GPU against CUDA's correctly rounded
-operations: the quotient v / s (reciprocal of the fp16 scale + two residual
-corrections) against __fdiv_rn for every positive finite fp16 scale with
+operations: the quotient v / s (reciprocal of the fp16 scale + one residual
+correction) against __fdiv_rn for every positive finite fp16 scale with
 65,536 values each, concentrated where rounding decisions are made; the
 reciprocal itself against __frcp_rn for every fp16 scale; and the block scale
 fp16(absmax / Qmax) for every fp32 absmax in [2^-100, 2^100) and every Qmax."""
