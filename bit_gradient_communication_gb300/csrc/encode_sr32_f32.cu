@@ -1,0 +1,9 @@
+// Stochastic encoder without error feedback, 32 elements per thread, for f32 gradients.
+#include "encode_sr32.cuh"
+
+namespace bitscom {
+cudaError_t launch_encode32_sr_f32(const EncArgs& a, int bits, cudaStream_t st)
+{
+    return encode32_sr_bits<0>(a, bits, st);
+}
+}  // namespace bitscom

@@ -94,6 +94,17 @@ struct SumArgs {
 // Rank-ordered fp32 sum; dtype 0 = fp32, 1 = bf16 inputs.
 cudaError_t launch_sum_ranks(const SumArgs& a, int dtype, cudaStream_t st);
 
+// The stochastic encoder without error feedback of 2-, 4- and 8-bit codes with
+// 32 elements per thread (encode_sr32.cuh): blocks of 32 .. 1024 elements, no
+// rotation, codes aligned to one thread's store (4 * bits bytes).
+inline bool encode32_sr_fits(const EncArgs& a, int bits)
+{
+    return a.hadamard == 0 && a.log2B >= 5 && a.log2B <= 10 && a.n < ((int64_t)1 << 42) &&
+           (reinterpret_cast<uintptr_t>(a.codes) & (uintptr_t)(4 * bits - 1)) == 0;
+}
+cudaError_t launch_encode32_sr_f32(const EncArgs& a, int bits, cudaStream_t st);
+cudaError_t launch_encode32_sr_bf16(const EncArgs& a, int bits, cudaStream_t st);
+
 // Return cudaErrorNotSupported for a combination without a kernel.
 cudaError_t launch_encode_f32(const EncArgs& a, int bits, bool sr, cudaStream_t st);
 cudaError_t launch_encode_bf16(const EncArgs& a, int bits, bool sr, cudaStream_t st);

@@ -106,6 +106,48 @@ def test_encoder_sr_alignment_paths(bits, dt):
         assert np.array_equal(scales.cpu().numpy().view(np.uint16), s_ref), f"offset {offset}"
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("block", [32, 64, 128, 256, 512, 1024])
+def test_sr_encoder_32_per_thread_paths(dt, bits, block):
+    # Stochastic rounding without error feedback of 2-, 4- and 8-bit codes in
+    # blocks of 32 .. 1024 takes an encoder with 32 elements per thread
+    # (8192-element rows).  Its straight-line form covers index offsets that
+    # are multiples of 4, normal scales and elements of magnitude 2^-96 or
+    # more; a thread's row with anything else is redone on the general path.
+    # Rows on both paths, full rows and a ragged last one, offsets on both
+    # sides of a Philox counter carry, and code pointers aligned for it (4b
+    # bytes) and for the 16-element encoder only (2b) must all give the
+    # oracle's bits.
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(bits * 100 + block)
+    R = 8192
+    n = 5 * R + 3 * 1024 + 40
+    x = rng.laplace(0.0, 1e-3, n).astype(np.float32)
+    x[R + 5] = 1e-35                                  # 0 < |v| < 2^-96
+    x[2 * R + 64] = 0.0
+    x[3 * R + 7 * 32 + 1] = -0.0
+    b0 = (4 * R) // block                             # a subnormal (or zero) scale, then a saturated one
+    x[b0 * block:(b0 + 1) * block] *= np.float32(1e-3)
+    x[(b0 + 1) * block:(b0 + 2) * block] *= np.float32(1e11)
+    xh = x if dt == "f32" else bf16_bits_of(torch, x)
+    xg = torch.from_numpy(xh).cuda() if dt == "f32" else torch.from_numpy(xh.view(np.int16)).cuda().view(torch.bfloat16)
+    nb = bc.packed_bytes(n, bits, block)
+    for off in (0, 4 * 12345, (1 << 34) - R - 64, 2):
+        p = bc.QParams(bits, block, bc.SR, seed=0xC0FFEE + off, index_offset=off)
+        c_ref, s_ref = O.quantize_pack(xh, O.params(bits, block, O.SR, seed=p.seed, index_offset=off))
+        for shift in (0, 2 * bits):
+            buf = torch.zeros(nb + 64, dtype=torch.uint8, device="cuda")
+            codes = buf[shift:shift + nb]
+            scales = torch.zeros(bc.num_blocks(n, block), dtype=torch.int16, device="cuda")
+            bc.quantize_pack(xg, p, None, codes, scales)
+            torch.cuda.synchronize()
+            tag = f"offset {off} code shift {shift}"
+            assert codes.cpu().numpy().tobytes() == c_ref.tobytes(), tag
+            assert np.array_equal(scales.cpu().numpy().view(np.uint16), s_ref), tag
+            assert not buf[:shift].any() and not buf[shift + nb:].any(), tag
+
+
 def test_encoder_special_blocks():
     # zero blocks, underflowing and subnormal scales, saturation, negative zero
     torch, bc = need_gpu()
