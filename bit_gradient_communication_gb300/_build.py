@@ -27,7 +27,7 @@ CU_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-fmad=false", "-Xcompiler"
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-Wall", "-I", INCLUDE, "-I", CSRC,
              "-I", os.path.join(CUDA_HOME, "include")]
 
-CU_SOURCES = ["encode_f32.cu", "encode_bf16.cu", "encode_sr32_f32.cu", "encode_sr32_bf16.cu", "decode_few.cu", "decode_w8.cu", "decode_many.cu", "dequant.cu", "qwd.cu", "noalloc.cu", "sum_ranks.cu"]
+CU_SOURCES = ["encode_f32.cu", "encode_bf16.cu", "encode_sr32_f32.cu", "encode_sr32_bf16.cu", "encode_sr32_f32_wide.cu", "encode_sr32_bf16_wide.cu", "decode_few.cu", "decode_w8.cu", "decode_many.cu", "dequant.cu", "qwd.cu", "noalloc.cu", "sum_ranks.cu"]
 CXX_SOURCES = ["api.cpp", "sched.cpp"]
 
 

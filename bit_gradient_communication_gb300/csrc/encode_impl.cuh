@@ -419,9 +419,13 @@ static cudaError_t run_encode_h(const EncArgs& a, cudaStream_t st)
 template <int IN, int BITS, bool EF, bool SR>
 static cudaError_t run_encode(const EncArgs& a, cudaStream_t st)
 {
-    if constexpr (SR && !EF && (BITS == 2 || BITS == 4 || BITS == 8)) {
-        if (encode32_sr_fits(a, BITS))
-            return IN == 0 ? launch_encode32_sr_f32(a, BITS, st) : launch_encode32_sr_bf16(a, BITS, st);
+    if constexpr (SR && !EF && BITS >= 2) {
+        if (encode32_sr_fits(a, BITS)) {
+            if constexpr (BITS >= 12)
+                return IN == 0 ? launch_encode32_sr_f32_wide(a, BITS, st) : launch_encode32_sr_bf16_wide(a, BITS, st);
+            else
+                return IN == 0 ? launch_encode32_sr_f32(a, BITS, st) : launch_encode32_sr_bf16(a, BITS, st);
+        }
     }
     // without error feedback only: with it, the 16-element layout spills and
     // measured slower on the 25 MiB fp32 buckets (0.59-0.64 vs 0.65-0.70)

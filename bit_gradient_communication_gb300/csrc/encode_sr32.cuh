@@ -1,5 +1,5 @@
 // encode_sr32.cuh -- the stochastic-rounding encoder without error feedback,
-// 32 elements per thread, for 2-, 4- and 8-bit codes and blocks of 32 to 1024
+// 32 elements per thread, for 2- to 16-bit codes and blocks of 32 to 4096
 // elements (bitscom README, "Implemented Features": blockwise quantization
 // with per-block FP16 scales, stochastic rounding support).
 //
@@ -112,18 +112,34 @@ __device__ __forceinline__ void put_piece(uint32_t (&cw)[BITS], int p, const Pac
     if constexpr (BITS == 2) {
         if (p & 1) cw[p >> 1] |= c.w[0] << 16;
         else cw[p >> 1] = c.w[0] & 0xFFFFu;
-    } else if constexpr (BITS == 4) {
-        cw[p] = c.w[0];
     } else {
-        cw[2 * p] = c.w[0];
-        cw[2 * p + 1] = c.w[1];
+        constexpr int K = BITS / 4;            // words per piece: 1, 2, 3 or 4
+#pragma unroll
+        for (int k = 0; k < K; ++k) cw[K * p + k] = c.w[k];
+    }
+}
+
+// Store two pieces' codes (16 elements) of 12 or 16 bits: 24 bytes at an
+// 8-byte boundary, or 32 at a 16-byte one.
+template <int BITS>
+__device__ __forceinline__ void store_two_pieces(uint8_t* p, const Packed<BITS>& c0, const Packed<BITS>& c1)
+{
+    if constexpr (BITS == 12) {
+        uint2* o = reinterpret_cast<uint2*>(p);
+        o[0] = make_uint2(c0.w[0], c0.w[1]);
+        o[1] = make_uint2(c0.w[2], c1.w[0]);
+        o[2] = make_uint2(c1.w[1], c1.w[2]);
+    } else {
+        uint4* o = reinterpret_cast<uint4*>(p);
+        o[0] = make_uint4(c0.w[0], c0.w[1], c0.w[2], c0.w[3]);
+        o[1] = make_uint4(c1.w[0], c1.w[1], c1.w[2], c1.w[3]);
     }
 }
 
 // One thread's row: elements e0 .. e0+31, a team of TW threads per block;
 // PART: the last, partial row (stores only within the blocks).
 template <int IN, int BITS, int TW, bool PART>
-__device__ __forceinline__ void sr32_row(const EncArgs& a, const RowIn32<IN>& r, uint64_t e0)
+__device__ __forceinline__ void sr32_row(const EncArgs& a, const RowIn32<IN>& r, uint64_t e0, float* red)
 {
     float v[32];
     if constexpr (IN == 0) {
@@ -149,8 +165,25 @@ __device__ __forceinline__ void sr32_row(const EncArgs& a, const RowIn32<IN>& r,
         mx = max3f(mx, fabsf(v[j]), fabsf(v[j + 1]));
         mn = min3f(mn, fabsf(v[j]), fabsf(v[j + 1]));
     }
-    const float stat = butterfly<false, TW>(fmaxf(mx, fabsf(v[31])));
+    float stat = fmaxf(mx, fabsf(v[31]));
     mn = fminf(mn, fabsf(v[31]));
+    if constexpr (TW <= 16) {
+        stat = butterfly<false, TW>(stat);
+    } else {
+        // the maximum of non-negative floats is that of their bit patterns
+        stat = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(stat)));
+        if constexpr (TW > 32) {
+            // teams of TW/32 warps: per-warp maxima through shared memory
+            // (red: this row's slots), one named barrier per team (ids 1..)
+            constexpr int kWarpsPerTeam = TW / 32;
+            const int team = threadIdx.x / TW;
+            if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = stat;
+            asm volatile("bar.sync %0, %1;" :: "r"(1 + team), "n"(TW) : "memory");
+            stat = red[team * kWarpsPerTeam];
+#pragma unroll
+            for (int k = 1; k < kWarpsPerTeam; ++k) stat = fmaxf(stat, red[team * kWarpsPerTeam + k]);
+        }
+    }
     const __half sh = block_scale<BITS>(stat, 1 << a.log2B);
     const float s = __half2float(sh);
     const float y = scale_reciprocal(s);
@@ -158,8 +191,15 @@ __device__ __forceinline__ void sr32_row(const EncArgs& a, const RowIn32<IN>& r,
     // Philox words and packed codes, elements 16h .. 16h+15: the one-sided
     // clamp (quantize8_sr_packed) when every scale of the warp allows it,
     // else the two-sided one (quantize8_sr_clamped); the choice is uniform
-    // over the warp, so the branch does not diverge
-    uint32_t cw[BITS];
+    // over the warp, so the branch does not diverge.  Codes of up to 8 bits
+    // are collected and stored at the end of the row; 12- and 16-bit codes
+    // (the two-sided clamp always) are stored per 16 elements, which keeps
+    // fewer registers live, and stored again if the row is redone.
+    // (the destination is formed where it is used: kept live across the
+    // quantisation it cost the narrow codes ~1.5 %)
+    auto write = [&]() { return !PART || (int64_t)e0 < (a.nb << a.log2B); };
+    auto out = [&]() { return a.codes + (e0 >> 3) * BITS; };
+    uint32_t cw[BITS <= 8 ? BITS : 1];
     auto quantize_row = [&](auto two_sided) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -175,18 +215,24 @@ __device__ __forceinline__ void sr32_row(const EncArgs& a, const RowIn32<IN>& r,
                 v1[j] = v[16 * h + 8 + j];
             }
             Packed<BITS> c0, c1;
-            if constexpr (decltype(two_sided)::value) {
+            if constexpr (decltype(two_sided)::value || BITS >= 12) {
                 quantize8_sr_clamped<BITS>(v0, s, y, rw0, a.pack_mul, c0);
                 quantize8_sr_clamped<BITS>(v1, s, y, rw1, a.pack_mul, c1);
             } else {
                 quantize8_sr_packed<BITS>(v0, s, y, rw0, false, a.pack_mul, c0);
                 quantize8_sr_packed<BITS>(v1, s, y, rw1, false, a.pack_mul, c1);
             }
-            put_piece<BITS>(cw, 2 * h, c0);
-            put_piece<BITS>(cw, 2 * h + 1, c1);
+            if constexpr (BITS <= 8) {
+                put_piece<BITS>(cw, 2 * h, c0);
+                put_piece<BITS>(cw, 2 * h + 1, c1);
+            } else if (write()) {
+                store_two_pieces<BITS>(out() + 2 * h * BITS, c0, c1);
+            }
         }
     };
-    if (__all_sync(0xFFFFFFFFu, s >= one_sided_min_scale<BITS>() && s < 65504.0f)) {
+    if constexpr (BITS >= 12) {
+        quantize_row(std::true_type{});
+    } else if (__all_sync(0xFFFFFFFFu, s >= one_sided_min_scale<BITS>() && s < 65504.0f)) {
         quantize_row(std::false_type{});
     } else {
         quantize_row(std::true_type{});
@@ -203,18 +249,25 @@ __device__ __forceinline__ void sr32_row(const EncArgs& a, const RowIn32<IN>& r,
             for (int j = 0; j < 8; ++j) vp[j] = v[8 * p + j];
             Packed<BITS> c;
             quantize8<BITS, true>(vp, s, y, rw, c, q);
-            put_piece<BITS>(cw, p, c);
+            if constexpr (BITS <= 8) {
+                put_piece<BITS>(cw, p, c);
+            } else if (write()) {
+                uint32_t* o = reinterpret_cast<uint32_t*>(out() + p * BITS);
+#pragma unroll
+                for (int k = 0; k < BITS / 4; ++k) o[k] = c.w[k];
+            }
         }
     }
-    if (!PART || (int64_t)e0 < (a.nb << a.log2B)) {
-        uint8_t* p = a.codes + (e0 >> 3) * BITS;
-        if constexpr (BITS == 2) {
-            *reinterpret_cast<uint2*>(p) = make_uint2(cw[0], cw[1]);
-        } else if constexpr (BITS == 4) {
-            *reinterpret_cast<uint4*>(p) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        } else {
-            reinterpret_cast<uint4*>(p)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-            reinterpret_cast<uint4*>(p)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    if constexpr (BITS <= 8) {
+        if (write()) {
+            uint8_t* const o = out();
+            if constexpr (BITS == 2) {
+                *reinterpret_cast<uint2*>(o) = make_uint2(cw[0], cw[1]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < BITS / 4; ++k)
+                    reinterpret_cast<uint4*>(o)[k] = make_uint4(cw[4 * k], cw[4 * k + 1], cw[4 * k + 2], cw[4 * k + 3]);
+            }
         }
     }
     const int64_t blk = (int64_t)(e0 >> a.log2B);
@@ -230,16 +283,20 @@ __global__ void __launch_bounds__(kThreads32, 2) encode32_sr_kernel(const EncArg
     const uint64_t step = (uint64_t)G * kRow32;
     int row = blockIdx.x;
     uint64_t e0 = (uint64_t)row * kRow32 + threadIdx.x * 32;
+    // per-warp maxima of teams wider than a warp: one set of slots per
+    // alternate row, a third for the partial row (a warp may reach the next
+    // row's exchange only after every warp of its team has read this one's)
+    __shared__ float red[3][kThreads32 / 32];
     RowIn32<IN> ra, rb;
     if (row < full) load_full32<IN>(a, e0, ra);
     while (row < full) {
         if (row + G < full) load_full32<IN>(a, e0 + step, rb);
-        sr32_row<IN, BITS, TW, false>(a, ra, e0);
+        sr32_row<IN, BITS, TW, false>(a, ra, e0, red[0]);
         row += G;
         e0 += step;
         if (row >= full) break;
         if (row + G < full) load_full32<IN>(a, e0 + step, ra);
-        sr32_row<IN, BITS, TW, false>(a, rb, e0);
+        sr32_row<IN, BITS, TW, false>(a, rb, e0, red[1]);
         row += G;
         e0 += step;
     }
@@ -247,7 +304,7 @@ __global__ void __launch_bounds__(kThreads32, 2) encode32_sr_kernel(const EncArg
     if (a.n % kRow32 != 0 && full % G == (int)blockIdx.x) {
         const uint64_t ep = (uint64_t)full * kRow32 + threadIdx.x * 32;
         load_part32<IN>(a, ep, ra);
-        sr32_row<IN, BITS, TW, true>(a, ra, ep);
+        sr32_row<IN, BITS, TW, true>(a, ra, ep, red[2]);
     }
 }
 
@@ -272,7 +329,7 @@ static cudaError_t run_encode32_tw(const EncArgs& a, cudaStream_t st)
     return cudaGetLastError();
 }
 
-// Launch for blocks of 32 .. 1024 elements (encode32_sr_fits, launch.h).
+// Launch for blocks of 32 .. 4096 elements (encode32_sr_fits, launch.h).
 template <int IN, int BITS>
 static cudaError_t run_encode32_sr(const EncArgs& a, cudaStream_t st)
 {
@@ -283,17 +340,31 @@ static cudaError_t run_encode32_sr(const EncArgs& a, cudaStream_t st)
     case 8: return run_encode32_tw<IN, BITS, 8>(a, st);
     case 9: return run_encode32_tw<IN, BITS, 16>(a, st);
     case 10: return run_encode32_tw<IN, BITS, 32>(a, st);
+    case 11: return run_encode32_tw<IN, BITS, 64>(a, st);
+    case 12: return run_encode32_tw<IN, BITS, 128>(a, st);
     default: return cudaErrorNotSupported;
     }
 }
 
+// 2-, 4- and 8-bit codes, and 12- and 16-bit codes: instantiated in separate
+// translation units (compile time).
 template <int IN>
-static cudaError_t encode32_sr_bits(const EncArgs& a, int bits, cudaStream_t st)
+static cudaError_t encode32_sr_bits_narrow(const EncArgs& a, int bits, cudaStream_t st)
 {
     switch (bits) {
     case 2: return run_encode32_sr<IN, 2>(a, st);
     case 4: return run_encode32_sr<IN, 4>(a, st);
     case 8: return run_encode32_sr<IN, 8>(a, st);
+    default: return cudaErrorNotSupported;
+    }
+}
+
+template <int IN>
+static cudaError_t encode32_sr_bits_wide(const EncArgs& a, int bits, cudaStream_t st)
+{
+    switch (bits) {
+    case 12: return run_encode32_sr<IN, 12>(a, st);
+    case 16: return run_encode32_sr<IN, 16>(a, st);
     default: return cudaErrorNotSupported;
     }
 }

@@ -94,16 +94,19 @@ struct SumArgs {
 // Rank-ordered fp32 sum; dtype 0 = fp32, 1 = bf16 inputs.
 cudaError_t launch_sum_ranks(const SumArgs& a, int dtype, cudaStream_t st);
 
-// The stochastic encoder without error feedback of 2-, 4- and 8-bit codes with
-// 32 elements per thread (encode_sr32.cuh): blocks of 32 .. 1024 elements, no
-// rotation, codes aligned to one thread's store (4 * bits bytes).
+// The stochastic encoder without error feedback with 32 elements per thread
+// (encode_sr32.cuh): 2- to 16-bit codes, blocks of 32 .. 4096 elements, no
+// rotation, codes aligned for one thread's stores (8 bytes at 2 bits, else 16).
 inline bool encode32_sr_fits(const EncArgs& a, int bits)
 {
-    return a.hadamard == 0 && a.log2B >= 5 && a.log2B <= 10 && a.n < ((int64_t)1 << 42) &&
-           (reinterpret_cast<uintptr_t>(a.codes) & (uintptr_t)(4 * bits - 1)) == 0;
+    const uintptr_t align = bits == 2 ? 8 : 16;
+    return bits >= 2 && a.hadamard == 0 && a.log2B >= 5 && a.log2B <= 12 && a.n < ((int64_t)1 << 42) &&
+           (reinterpret_cast<uintptr_t>(a.codes) & (align - 1)) == 0;
 }
-cudaError_t launch_encode32_sr_f32(const EncArgs& a, int bits, cudaStream_t st);
+cudaError_t launch_encode32_sr_f32(const EncArgs& a, int bits, cudaStream_t st);        // 2, 4, 8 bits
 cudaError_t launch_encode32_sr_bf16(const EncArgs& a, int bits, cudaStream_t st);
+cudaError_t launch_encode32_sr_f32_wide(const EncArgs& a, int bits, cudaStream_t st);   // 12, 16 bits
+cudaError_t launch_encode32_sr_bf16_wide(const EncArgs& a, int bits, cudaStream_t st);
 
 // Return cudaErrorNotSupported for a combination without a kernel.
 cudaError_t launch_encode_f32(const EncArgs& a, int bits, bool sr, cudaStream_t st);

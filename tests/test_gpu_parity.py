@@ -107,18 +107,19 @@ def test_encoder_sr_alignment_paths(bits, dt):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("bits", [2, 4, 8])
-@pytest.mark.parametrize("block", [32, 64, 128, 256, 512, 1024])
+@pytest.mark.parametrize("bits", [2, 4, 8, 12, 16])
+@pytest.mark.parametrize("block", [32, 64, 128, 256, 512, 1024, 2048, 4096])
 def test_sr_encoder_32_per_thread_paths(dt, bits, block):
-    # Stochastic rounding without error feedback of 2-, 4- and 8-bit codes in
-    # blocks of 32 .. 1024 takes an encoder with 32 elements per thread
-    # (8192-element rows).  Its straight-line form covers index offsets that
-    # are multiples of 4, normal scales and elements of magnitude 2^-96 or
-    # more; a thread's row with anything else is redone on the general path.
-    # Rows on both paths, full rows and a ragged last one, offsets on both
-    # sides of a Philox counter carry, and code pointers aligned for it (4b
-    # bytes) and for the 16-element encoder only (2b) must all give the
-    # oracle's bits.
+    # Stochastic rounding without error feedback of 2- to 16-bit codes in
+    # blocks of 32 .. 4096 takes an encoder with 32 elements per thread
+    # (8192-element rows; blocks of 2048 and 4096 reduce across warps).  Its
+    # straight-line form covers index offsets that are multiples of 4 and
+    # elements of magnitude 2^-96 or more, with a one- or two-sided clamp
+    # chosen per warp from the scales; a thread's row with anything else is
+    # redone on the general path.  Rows on both paths, full rows and a ragged
+    # last one, subnormal and saturated scales, offsets on both sides of a
+    # Philox counter carry, and code pointers aligned for it and only for the
+    # older encoders (shifted by 2b bytes) must all give the oracle's bits.
     torch, bc = need_gpu()
     rng = np.random.default_rng(bits * 100 + block)
     R = 8192
