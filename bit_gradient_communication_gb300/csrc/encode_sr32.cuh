@@ -15,11 +15,11 @@
 //     the one-sided clamp with the packed-word fix (quantize8_sr_packed)
 //     where every scale of the warp is at least one_sided_min_scale and
 //     below 65504, else the two-sided clamp (quantize8_sr_clamped), chosen
-//     per warp.  The cases neither covers -- an element with 0 < |v| < 2^-96
-//     (the test, on the smallest magnitude, also takes zeros), an index
-//     offset not a multiple of 4, a Philox counter whose low word wraps inside
-//     the thread's run -- are tested together at the end of the row, which is
-//     then recomputed on the general path (random_words8, quantize8);
+//     per warp.  The cases neither covers -- an element with 0 < |v| < 2^-96,
+//     an index offset not a multiple of 4, a Philox counter whose low word
+//     wraps inside the thread's run -- are tested together at the end of the
+//     row, which is then recomputed on the general path (random_words8,
+//     quantize8);
 //   * 32 elements per thread (8192-element rows of a 256-thread CTA) spread
 //     the per-row work (team butterfly, scale and reciprocal, the rare-case
 //     test, addresses, the scale store) over twice the elements of
@@ -237,8 +237,15 @@ __device__ __forceinline__ void sr32_row(const EncArgs& a, const RowIn32<IN>& r,
     } else {
         quantize_row(std::true_type{});
     }
-    const bool rare = (mn < 0x1p-96f) | (((uint32_t)i0 & 3u) != 0) | ((uint32_t)g > 0xFFFFFFF8u);
-    if (rare) {
+    // the smallest magnitude also flags zeros, which the fast quotient divides
+    // exactly: rows flagged only by zeros keep their codes
+    const bool words_off = (((uint32_t)i0 & 3u) != 0) | ((uint32_t)g > 0xFFFFFFF8u);
+    bool redo = words_off;
+    if (mn < 0x1p-96f) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) redo |= fabsf(v[j]) < 0x1p-96f && v[j] != 0.0f;
+    }
+    if (redo) {
         const uint32_t shift = (uint32_t)i0 & 3u;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {

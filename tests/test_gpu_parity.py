@@ -126,8 +126,10 @@ def test_sr_encoder_32_per_thread_paths(dt, bits, block):
     n = 5 * R + 3 * 1024 + 40
     x = rng.laplace(0.0, 1e-3, n).astype(np.float32)
     x[R + 5] = 1e-35                                  # 0 < |v| < 2^-96
-    x[2 * R + 64] = 0.0
+    x[R + 6] = 0.0                                    # a zero in the same thread's 32 elements
+    x[2 * R + 64] = 0.0                               # zeros alone keep the straight-line form
     x[3 * R + 7 * 32 + 1] = -0.0
+    x[2 * R + 1024:3 * R][rng.random(R - 1024) < 0.05] = 0.0
     b0 = (4 * R) // block                             # a subnormal (or zero) scale, then a saturated one
     x[b0 * block:(b0 + 1) * block] *= np.float32(1e-3)
     x[(b0 + 1) * block:(b0 + 2) * block] *= np.float32(1e11)
