@@ -50,16 +50,19 @@ DEC_BYTES_PER_ELEM = W_RANKS * (BITS / 8 + 2 / BLOCK) + 4 + 4 + BITS / 8 + 2 / B
 # DRAM traffic per element measured by ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum per launch / its elements), valid only while the
 # sources of the two kernels' translation units (TRAFFIC_SOURCES) hash to
-# `src`.  Captured on the same step with 2e8 elements per rank (each encoder
-# launch moves 2.1 GB, 16 times the L2), caches left alone between launches
-# (ncu --cache-control none), averaged over the step's 8 encoder and 8
-# decoder launches; the step's total equals its algorithmic bytes to 0.01 %,
-# and the full-size launches move the same bytes per element.
+# `src`.  Captured on the same step with 6e7 elements per rank (3.4 GB on the
+# device; each encoder launch moves 0.63 GB, five times the L2), caches left
+# alone between launches (ncu --cache-control none), averaged over the step's
+# 8 encoder and 8 decoder launches; the step's total equals its algorithmic
+# bytes to 0.04 % (the last encoder's dirty lines are written back, and
+# counted, during the first decoder), and the bytes per element do not depend
+# on the size once it is well above the L2 (2e8 per rank gave 10.5057 and
+# 12.6902 on earlier sources).
 TRAFFIC_SOURCES = ("launch.h", "codec.cuh", "encode_impl.cuh", "encode_bf16.cu", "decode_impl.cuh",
                    "decode_w8.cu")
 NCU_TRAFFIC = {
-    "encode": {"src": "5df02a2e4d3f31a9", "bytes_per_elem": 10.5057},
-    "decode": {"src": "5df02a2e4d3f31a9", "bytes_per_elem": 12.6902},
+    "encode": {"src": "7d6026e05ef4e817", "bytes_per_elem": 10.4914},
+    "decode": {"src": "7d6026e05ef4e817", "bytes_per_elem": 12.7933},
 }
 
 
