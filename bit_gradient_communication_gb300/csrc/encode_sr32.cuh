@@ -167,6 +167,11 @@ __device__ __forceinline__ void sr32_row(const EncArgs& a, const RowIn32<IN>& r,
     }
     float stat = fmaxf(mx, fabsf(v[31]));
     mn = fminf(mn, fabsf(v[31]));
+    // teams wider than a warp wait at a barrier below: the first Philox run
+    // goes before it, where it can overlap the exchange
+    constexpr bool kEarly = TW > 32;
+    uint4 w_early[kEarly ? 4 : 1];
+    if constexpr (kEarly) philox10_run<4>((uint32_t)g, (uint32_t)(g >> 32), a.keys, w_early);
     if constexpr (TW <= 16) {
         stat = butterfly<false, TW>(stat);
     } else {
@@ -205,7 +210,12 @@ __device__ __forceinline__ void sr32_row(const EncArgs& a, const RowIn32<IN>& r,
         for (int h = 0; h < 2; ++h) {
             uint4 w[4];
             const uint64_t gh = g + 4 * h;
-            philox10_run<4>((uint32_t)gh, (uint32_t)(gh >> 32), a.keys, w);
+            if (kEarly && h == 0) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) w[k] = w_early[kEarly ? k : 0];
+            } else {
+                philox10_run<4>((uint32_t)gh, (uint32_t)(gh >> 32), a.keys, w);
+            }
             const uint32_t rw0[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
             const uint32_t rw1[8] = {w[2].x, w[2].y, w[2].z, w[2].w, w[3].x, w[3].y, w[3].z, w[3].w};
             float v0[8], v1[8];
