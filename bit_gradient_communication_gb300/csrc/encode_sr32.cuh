@@ -15,7 +15,10 @@
 //     the one-sided clamp with the packed-word fix (quantize8_sr_packed)
 //     where every scale of the warp is at least one_sided_min_scale and
 //     below 65504, else the two-sided clamp (quantize8_sr_clamped), chosen
-//     per warp.  The cases neither covers -- an element with 0 < |v| < 2^-96,
+//     per warp (12- and 16-bit codes always take the two-sided one).  Teams
+//     of a warp or more reduce with redux.sync; wider teams add a per-team
+//     named barrier, and run their first Philox counters before it.  The
+//     cases neither quantiser covers -- an element with 0 < |v| < 2^-96,
 //     an index offset not a multiple of 4, a Philox counter whose low word
 //     wraps inside the thread's run -- are tested together at the end of the
 //     row, which is then recomputed on the general path (random_words8,
@@ -105,15 +108,17 @@ __device__ __forceinline__ constexpr float one_sided_min_scale()
     return (float)(1 << (BITS - 1)) * 0x1p-24f;
 }
 
-// Place piece p's packed codes (8 elements) into the thread's code words.
+// Place piece p's packed codes (8 elements) into the thread's code words
+// (codes of up to 8 bits; wider ones are stored as they are packed).
 template <int BITS>
 __device__ __forceinline__ void put_piece(uint32_t (&cw)[BITS], int p, const Packed<BITS>& c)
 {
+    static_assert(BITS <= 8, "codes of up to 8 bits");
     if constexpr (BITS == 2) {
         if (p & 1) cw[p >> 1] |= c.w[0] << 16;
         else cw[p >> 1] = c.w[0] & 0xFFFFu;
     } else {
-        constexpr int K = BITS / 4;            // words per piece: 1, 2, 3 or 4
+        constexpr int K = BITS / 4;            // words per piece: 1 or 2
 #pragma unroll
         for (int k = 0; k < K; ++k) cw[K * p + k] = c.w[k];
     }
