@@ -121,7 +121,10 @@ const char* bitscom_last_cuda_error(void);
  *   scales_out [num_blocks] fp16 bit patterns (2-byte aligned).
  * Buffers must not overlap.  Performance note: without error feedback a
  * codes_out aligned to twice the store width (and blocks of >= 16) lets the
- * encoder handle 16 elements per thread; the results are the same bits.
+ * encoder handle 16 elements per thread; with stochastic rounding, b >= 2,
+ * blocks of 32 .. 4096 and codes_out 16-byte aligned (8 at b = 2) it handles
+ * 32, which measured 1.2x faster (fp32, 4-bit, block 128).  The results are
+ * the same bits on every path.
  */
 bitscom_status bitscom_quantize_pack(const void* x, bitscom_dtype dt, int64_t n, float* err,
                                      const bitscom_qparams* p, void* codes_out,
