@@ -923,6 +923,18 @@ def run_workload(args):
         algo = wl.n * (2 + 8 + wl.bits / 8 + 2 / wl.block)
         extra = {"l2": "inputs larger than L2 (67 GB per step)" if not args.wl_n else "one pass per step",
                  "buckets": len(bc.plan_buckets(wl.n, 2, wl.block, wl.bucket_bytes)) - 1, "streams": 2}
+    elif args.workload == "local_sum_w8_gpt1p3b":
+        # pipeline-A's full-precision local reduce on the node leader: the fp32
+        # sum of the 8 local ranks' bf16 gradients in rank order
+        xs = [synth.gradients(wl.kind, wl.n, wl.seed + w, dtype=dt, **wl.params) for w in range(wl.ranks)]
+        out_sum = torch.empty(wl.n, device="cuda")
+        step = lambda: bc.sum_ranks(xs, out=out_sum)
+        for _ in range(warm):
+            step()
+        t = _timed(torch, step, K)
+        algo = wl.n * (wl.ranks * 2 + 4)
+        extra = {"l2": "inputs larger than L2 (26 GB per step)", "ranks": wl.ranks, "output": "fp32"}
+        wl_elems = wl.n * wl.ranks
     else:
         raise SystemExit(f"workload {args.workload}: use the default run")
     gbs = algo / t / 1e6

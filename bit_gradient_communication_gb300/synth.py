@@ -116,4 +116,8 @@ WORKLOADS = {
                                          {"sigma": 1e-3}, bits=4, block=128, ranks=8, seed=1000),
     "sweep_laplace_256m": Workload("sweep_laplace_256m", 268_435_456, "f32", "laplace", {"b": 1e-3},
                                    bits=4, block=128, seed=5, sr_seed=55),
+    # pipeline-A without local quantisation: the node leader's rank-ordered fp32
+    # sum of its 8 local ranks' GPT-1.3B-shaped gradients
+    "local_sum_w8_gpt1p3b": Workload("local_sum_w8_gpt1p3b", 1_300_000_000, "bf16", "normal", {"sigma": 1e-3},
+                                     ranks=8, seed=1000),
 }

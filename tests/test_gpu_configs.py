@@ -228,3 +228,27 @@ def test_sweep_laplace_256m_whole():
     assert total == n * len(SWEEP_BITS) * len(SWEEP_BLOCKS) * 2
     del x, deq, rt
     torch.cuda.empty_cache()
+
+
+def test_local_sum_w8_gpt1p3b_whole():
+    """Pipeline-A's full-precision local reduce at the bench's size: the fp32
+    rank-ordered sum of 8 local ranks' 1.3e9-element bf16 gradients, compared
+    with the oracle's sum on every element."""
+    _, bc = need_gpu()
+    from bit_gradient_communication_gb300 import synth
+    wl = synth.WORKLOADS["local_sum_w8_gpt1p3b"]
+    n = wl.n
+    xs = [synth.gradients(wl.kind, n, wl.seed + w, dtype=torch.bfloat16, **wl.params) for w in range(wl.ranks)]
+    out = torch.empty(n, device="cuda")
+    bc.sum_ranks(xs, out=out)
+    torch.cuda.synchronize()
+
+    def fetch(lo, hi):
+        return [_bits16(x[lo:hi]) for x in xs], _f32(out[lo:hi])
+
+    def check(lo, hi, d):
+        assert whole_check.same_bits(O.sum_ranks(d[0]), d[1]), f"sum at {lo}"
+
+    assert whole_check.run(whole_check.slices(n, 1 << 22), fetch, check) == n
+    del xs, out
+    torch.cuda.empty_cache()

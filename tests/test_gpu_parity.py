@@ -784,7 +784,7 @@ def test_decoder_maximum_ranks(bits):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("W", [1, 2, 3, 8, 64])
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 8, 64])
 def test_sum_ranks_matches_oracle(dt, W):
     # The full-precision local reduce: rank-ordered fp32 sum, bit for bit,
     # with values that tie (2^24 + 1) and zeros of both signs mixed in.
