@@ -935,6 +935,25 @@ def run_workload(args):
         algo = wl.n * (wl.ranks * 2 + 4)
         extra = {"l2": "inputs larger than L2 (26 GB per step)", "ranks": wl.ranks, "output": "fp32"}
         wl_elems = wl.n * wl.ranks
+    elif args.workload == "local_decode_w8_gpt1p3b":
+        # pipeline-A's local stage with local quantisation, on the node leader:
+        # the 8 local ranks' 4-bit codes decoded into their rank-ordered fp32 sum
+        p = bc.QParams(wl.bits, wl.block)
+        cs, ss = [], []
+        for w in range(wl.ranks):
+            x = synth.gradients(wl.kind, wl.n, wl.seed + w, dtype=dt, **wl.params)
+            c, s_ = bc.quantize_pack(x, p)
+            cs.append(c)
+            ss.append(s_)
+            del x
+        out_sum = torch.empty(wl.n, device="cuda")
+        step = lambda: bc.unpack_dequant_reduce_requant(cs, ss, wl.n, p, sum_out=out_sum)
+        for _ in range(warm):
+            step()
+        t = _timed(torch, step, K)
+        algo = wl.n * (wl.ranks * (wl.bits / 8 + 2 / wl.block) + 4)
+        extra = {"l2": "inputs larger than L2 (5.3 GB of codes per call)", "ranks": wl.ranks, "output": "fp32 sum"}
+        wl_elems = wl.n * wl.ranks
     else:
         raise SystemExit(f"workload {args.workload}: use the default run")
     gbs = algo / t / 1e6

@@ -238,14 +238,16 @@ decode_kernel(const DecArgs a)
 // sides; otherwise decode_kernel runs.
 // ---------------------------------------------------------------------------
 
-template <bool SR>
+// REQ = false: the rank sum alone (no requantisation, no stage-2 error): the
+// leader's decode of pipeline-A with local quantisation.
+template <bool SR, bool REQ = true>
 __global__ void __launch_bounds__(kThreads16, 3) decode16_w8_kernel(const DecArgs a)
 {
     __shared__ float red[2][kThreads16 / 32];
     const int64_t n = a.n;
     const int rows = (int)((n + kRow - 1) / kRow);       // < 2^31 (decode16_fits)
     const int tid = threadIdx.x;
-    const Team team = make_team16(a.log2Bout);
+    const Team team = make_team16(REQ ? a.log2Bout : 4);
 
     uint2 cc[8];
     uint32_t sc[4];                                  // the 8 ranks' fp16 scales, two per word
@@ -282,6 +284,17 @@ __global__ void __launch_bounds__(kThreads16, 3) decode16_w8_kernel(const DecArg
             }
         }
         if (row + (int)gridDim.x < rows) load(row + gridDim.x);   // overlaps the requantisation
+        if constexpr (!REQ) {
+            if (valid == 16) {
+                st8_f32(a.sum_out + e0, lo);
+                st8_f32(a.sum_out + e0 + 8, hi);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (j < valid) a.sum_out[e0 + j] = j < 8 ? lo[j] : hi[j - 8];
+            }
+            continue;
+        }
         // the stage-2 error is loaded only now, after the next row's codes are
         // in flight: issued at the top of the row it held 16 registers through
         // the accumulation and measured 8 % slower (0.341 vs 0.317 ms per chunk)
@@ -364,7 +377,7 @@ __global__ void __launch_bounds__(kThreads16, 3) decode16_w8_kernel(const DecArg
     }
 }
 
-template <bool SR>
+template <bool SR, bool REQ = true>
 static cudaError_t run_decode16_w8(const DecArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};
@@ -374,13 +387,25 @@ static cudaError_t run_decode16_w8(const DecArgs& a, cudaStream_t st)
         int dev = 0, occ = 0, sms = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode16_w8_kernel<SR>, kThreads16, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode16_w8_kernel<SR, REQ>, kThreads16, 0);
         c = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
         cap.store(c, std::memory_order_relaxed);
     }
     const int grid = (int)(rows < c ? rows : c);
-    decode16_w8_kernel<SR><<<grid, kThreads16, 0, st>>>(a);
+    decode16_w8_kernel<SR, REQ><<<grid, kThreads16, 0, st>>>(a);
     return cudaGetLastError();
+}
+
+// The rank sum alone through decode16_w8_kernel: eight ranks of 4-bit codes
+// in blocks of >= 16, 8-byte aligned code pointers, a sum output.
+static bool decode16_sum_fits(const DecArgs& a)
+{
+    if (a.W != 8 || a.log2Bin < 4 || a.sum_out == nullptr || a.codes_out != nullptr || a.err2 != nullptr ||
+        a.n >= ((int64_t)1 << 42))
+        return false;
+    for (int k = 0; k < 8; ++k)
+        if ((reinterpret_cast<uintptr_t>(a.codes[k]) & 7u) != 0) return false;
+    return true;
 }
 
 static bool decode16_fits(const DecArgs& a)
@@ -397,6 +422,9 @@ static cudaError_t run_decode_kw(const DecArgs& a, cudaStream_t st)
 {
     if constexpr (KW == 8 && BIN == 4 && BOUT == 4 && !MANY) {
         if (decode16_fits(a)) return run_decode16_w8<SR>(a, st);
+    }
+    if constexpr (KW == 8 && BIN == 4 && BOUT == 0 && !MANY) {
+        if (decode16_sum_fits(a)) return run_decode16_w8<false, false>(a, st);
     }
     static std::atomic<int> cap{0};
     const int64_t rows = (a.n + kRow - 1) / kRow;

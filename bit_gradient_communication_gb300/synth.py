@@ -120,4 +120,8 @@ WORKLOADS = {
     # sum of its 8 local ranks' GPT-1.3B-shaped gradients
     "local_sum_w8_gpt1p3b": Workload("local_sum_w8_gpt1p3b", 1_300_000_000, "bf16", "normal", {"sigma": 1e-3},
                                      ranks=8, seed=1000),
+    # pipeline-A with local quantisation: the node leader's decode of its 8 local
+    # ranks' 4-bit codes into their rank-ordered fp32 sum (no requantisation)
+    "local_decode_w8_gpt1p3b": Workload("local_decode_w8_gpt1p3b", 1_300_000_000, "bf16", "normal",
+                                        {"sigma": 1e-3}, bits=4, block=128, ranks=8, seed=1000),
 }

@@ -252,3 +252,44 @@ def test_local_sum_w8_gpt1p3b_whole():
     assert whole_check.run(whole_check.slices(n, 1 << 22), fetch, check) == n
     del xs, out
     torch.cuda.empty_cache()
+
+
+def test_local_decode_w8_gpt1p3b_whole():
+    """Pipeline-A's local stage with local quantisation at the bench's size: 8
+    local ranks' 1.3e9-element bf16 gradients encoded to 4-bit block-128 codes
+    and decoded by the leader into their rank-ordered fp32 sum.  Per slice the
+    oracle encodes every rank's gradient itself and sums the decoded values;
+    codes, scales and the sum are compared on every element."""
+    _, bc = need_gpu()
+    from bit_gradient_communication_gb300 import synth
+    wl = synth.WORKLOADS["local_decode_w8_gpt1p3b"]
+    n, b, B = wl.n, wl.bits, wl.block
+    p = bc.QParams(b, B)
+    xs, cs, ss = [], [], []
+    for w in range(wl.ranks):
+        x = synth.gradients(wl.kind, n, wl.seed + w, dtype=torch.bfloat16, **wl.params)
+        c, s = bc.quantize_pack(x, p)
+        xs.append(x)
+        cs.append(c)
+        ss.append(s)
+    out = torch.empty(n, device="cuda")
+    bc.unpack_dequant_reduce_requant(cs, ss, n, p, sum_out=out)
+    torch.cuda.synchronize()
+
+    def fetch(lo, hi):
+        return ([_bits16(x[lo:hi]) for x in xs], [_u8(c[lo * b // 8: hi * b // 8]) for c in cs],
+                [_u16(s[lo // B: hi // B]) for s in ss], _f32(out[lo:hi]))
+
+    def check(lo, hi, d):
+        op = O.params(b, B)
+        enc = [O.quantize_pack(x, op) for x in d[0]]
+        for w, (c, s) in enumerate(enc):
+            assert whole_check.same_bits(c, d[1][w]), f"rank {w} codes at {lo}"
+            assert whole_check.same_bits(s, d[2][w]), f"rank {w} scales at {lo}"
+        total, _, _ = O.unpack_dequant_reduce_requant([c for c, _ in enc], [s for _, s in enc], hi - lo, op,
+                                                      True, None, None)
+        assert whole_check.same_bits(total, d[3]), f"sum at {lo}"
+
+    assert whole_check.run(whole_check.slices(n, 1 << 22), fetch, check) == n
+    del xs, cs, ss, out
+    torch.cuda.empty_cache()
