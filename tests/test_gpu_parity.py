@@ -464,6 +464,11 @@ def test_decoder_w8_alignment_paths(offset, sr):
             assert np.array_equal(e2_g.cpu().numpy().view(np.uint32), e2_ref.view(np.uint32)), tag
             if with_sum:
                 assert np.array_equal(sm.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), tag
+            # the sum alone (no requantisation): the 16-element kernel without
+            # its requantisation, or the general decoder
+            sm2, _, _ = bc.unpack_dequant_reduce_requant(cin, sin, n, bc.QParams(4, B), sum_out=True)
+            torch.cuda.synchronize()
+            assert np.array_equal(sm2.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), tag + " sum only"
 
 
 @pytest.mark.parametrize("bin_blk,bout_blk", [(32, 512), (512, 32), (16, 4096), (4096, 16)])
