@@ -240,7 +240,27 @@ decode_kernel(const DecArgs a)
 
 // REQ = false: the rank sum alone (no requantisation, no stage-2 error): the
 // leader's decode of pipeline-A with local quantisation.
-template <bool SR, bool REQ = true>
+// TW > 0: blocks of 16 TW output elements (a team of TW threads), with the
+// requantisation as straight-line code (fixed-width butterfly, the clamp chosen
+// per warp); TW = 0 reads the team width at run time.
+template <int BITS>
+__device__ __forceinline__ void rtn8_levels(const float (&v)[8], float s, float y, bool clamp, Packed<BITS>& c,
+                                            float (&q)[8])
+{
+    constexpr float Q = (float)((1 << (BITS - 1)) - 1);
+    uint32_t mb[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float t = div_by_scale(v[j], s, y);
+        if (clamp) t = fminf(fmaxf(t, -Q), Q);
+        const float m = __fadd_rn(t, kMagic);                // 1.5*2^23 + rint(t)
+        q[j] = __fsub_rn(m, kMagic);
+        mb[j] = __float_as_uint(m);
+    }
+    pack8<BITS>(mb, c);
+}
+
+template <bool SR, bool REQ = true, int TW = 0>
 __global__ void __launch_bounds__(kThreads16, 3) decode16_w8_kernel(const DecArgs a)
 {
     __shared__ float red[2][kThreads16 / 32];
@@ -325,17 +345,46 @@ __global__ void __launch_bounds__(kThreads16, 3) decode16_w8_kernel(const DecArg
 
         // stage-2 error feedback, block statistic over 16 elements, requantise
         float v0[8], v1[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float x0 = lo[j], x1 = hi[j];
-            if (a.err2 != nullptr) { x0 = __fadd_rn(x0, e2[j]); x1 = __fadd_rn(x1, e2[j + 8]); }
-            v0[j] = j < valid ? x0 : 0.0f;
-            v1[j] = j + 8 < valid ? x1 : 0.0f;
-        }
         float stat = 0.0f;
+        if constexpr (TW > 0) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) stat = fmaxf(stat, fmaxf(fabsf(v0[j]), fabsf(v1[j])));
-        stat = team_reduce<false>(stat, team, red[parity]);
+            for (int j = 0; j < 8; ++j) {
+                v0[j] = lo[j];
+                v1[j] = hi[j];
+                if (a.err2 != nullptr) { v0[j] = __fadd_rn(v0[j], e2[j]); v1[j] = __fadd_rn(v1[j], e2[j + 8]); }
+            }
+            if (valid < 16) {                        // the last, partial row only
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j >= valid) v0[j] = 0.0f;
+                    if (j + 8 >= valid) v1[j] = 0.0f;
+                }
+            }
+            float mx = max3f(fabsf(v0[0]), fabsf(v0[1]), fabsf(v0[2]));
+            mx = max3f(mx, fabsf(v0[3]), fabsf(v0[4]));
+            mx = max3f(mx, fabsf(v0[5]), fabsf(v0[6]));
+            mx = max3f(mx, fabsf(v0[7]), fabsf(v1[0]));
+            mx = max3f(mx, fabsf(v1[1]), fabsf(v1[2]));
+            mx = max3f(mx, fabsf(v1[3]), fabsf(v1[4]));
+            mx = max3f(mx, fabsf(v1[5]), fabsf(v1[6]));
+            stat = fmaxf(mx, fabsf(v1[7]));
+            if constexpr (TW <= 16) {
+                stat = butterfly<false, TW>(stat);
+            } else {
+                stat = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(stat)));
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float x0 = lo[j], x1 = hi[j];
+                if (a.err2 != nullptr) { x0 = __fadd_rn(x0, e2[j]); x1 = __fadd_rn(x1, e2[j + 8]); }
+                v0[j] = j < valid ? x0 : 0.0f;
+                v1[j] = j + 8 < valid ? x1 : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) stat = fmaxf(stat, fmaxf(fabsf(v0[j]), fabsf(v1[j])));
+            stat = team_reduce<false>(stat, team, red[parity]);
+        }
         const int64_t blk = e0 >> a.log2Bout;
         const __half sh = block_scale<4>(stat, 1 << a.log2Bout);
         const float s2 = __half2float(sh);
@@ -352,8 +401,20 @@ __global__ void __launch_bounds__(kThreads16, 3) decode16_w8_kernel(const DecArg
         }
         Packed<4> c0, c1;
         float q0[8], q1[8];
-        quantize8<4, SR, false>(v0, s2, y2, rw0, c0, q0);
-        quantize8<4, SR, false>(v1, s2, y2, rw1, c1, q1);
+        if constexpr (TW > 0 && !SR) {
+            // no clamp where every scale of the warp is normal and below 65504
+            // (then |t| < Qmax + 1/2, see quantize8); a zero scale gives t = 0
+            if (__all_sync(0xFFFFFFFFu, s2 >= 0x1p-14f && s2 < 65504.0f)) {
+                rtn8_levels<4>(v0, s2, y2, false, c0, q0);
+                rtn8_levels<4>(v1, s2, y2, false, c1, q1);
+            } else {
+                rtn8_levels<4>(v0, s2, y2, true, c0, q0);
+                rtn8_levels<4>(v1, s2, y2, true, c1, q1);
+            }
+        } else {
+            quantize8<4, SR, false>(v0, s2, y2, rw0, c0, q0);
+            quantize8<4, SR, false>(v1, s2, y2, rw1, c1, q1);
+        }
         if (e0 < (a.nb_out << a.log2Bout))
             *reinterpret_cast<uint2*>(a.codes_out + (e0 >> 1)) = make_uint2(c0.w[0], c1.w[0]);
         if (team.lane == 0 && blk < a.nb_out) a.scales_out[blk] = __half_as_ushort(sh);
@@ -377,7 +438,7 @@ __global__ void __launch_bounds__(kThreads16, 3) decode16_w8_kernel(const DecArg
     }
 }
 
-template <bool SR, bool REQ = true>
+template <bool SR, bool REQ = true, int TW = 0>
 static cudaError_t run_decode16_w8(const DecArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};
@@ -387,12 +448,12 @@ static cudaError_t run_decode16_w8(const DecArgs& a, cudaStream_t st)
         int dev = 0, occ = 0, sms = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode16_w8_kernel<SR, REQ>, kThreads16, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode16_w8_kernel<SR, REQ, TW>, kThreads16, 0);
         c = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
         cap.store(c, std::memory_order_relaxed);
     }
     const int grid = (int)(rows < c ? rows : c);
-    decode16_w8_kernel<SR, REQ><<<grid, kThreads16, 0, st>>>(a);
+    decode16_w8_kernel<SR, REQ, TW><<<grid, kThreads16, 0, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -421,7 +482,17 @@ template <int BIN, int BOUT, bool SR, bool MANY, int KW>
 static cudaError_t run_decode_kw(const DecArgs& a, cudaStream_t st)
 {
     if constexpr (KW == 8 && BIN == 4 && BOUT == 4 && !MANY) {
-        if (decode16_fits(a)) return run_decode16_w8<SR>(a, st);
+        if (decode16_fits(a)) {
+            switch (a.log2Bout) {
+            case 4: return run_decode16_w8<SR, true, 1>(a, st);
+            case 5: return run_decode16_w8<SR, true, 2>(a, st);
+            case 6: return run_decode16_w8<SR, true, 4>(a, st);
+            case 7: return run_decode16_w8<SR, true, 8>(a, st);
+            case 8: return run_decode16_w8<SR, true, 16>(a, st);
+            case 9: return run_decode16_w8<SR, true, 32>(a, st);
+            default: return run_decode16_w8<SR>(a, st);
+            }
+        }
     }
     if constexpr (KW == 8 && BIN == 4 && BOUT == 0 && !MANY) {
         if (decode16_sum_fits(a)) return run_decode16_w8<false, false>(a, st);
