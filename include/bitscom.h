@@ -153,7 +153,9 @@ bitscom_status bitscom_quantize_pack(const void* x, bitscom_dtype dt, int64_t n,
  * two-level pair (8 -> 4); other pairs return BITSCOM_EUNSUPPORTED.
  * Performance note: for W = 8 and 4 -> 4 bits, 8-byte aligned codes_in and
  * codes_out (and blocks of >= 16) let the decoder handle 16 elements per
- * thread; the results are the same bits.
+ * thread, and so do 8-byte aligned codes_in for W = 8 4-bit codes decoded into
+ * sum_out alone (no p_out, no err2); W = 1 without p_out runs the all-gather-
+ * side decode with mul = 1.  The results are the same bits on every path.
  */
 bitscom_status bitscom_unpack_dequant_reduce_requant(
     const void* const* codes_in, const uint16_t* const* scales_in, int32_t W, int64_t n,
