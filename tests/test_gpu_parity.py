@@ -636,27 +636,77 @@ def test_allgather_decode_matches_oracle(bits, block, out):
         assert np.array_equal(got, ref.view(np.uint32 if out == "f32" else np.uint16)), f"n={n} mul={mul}"
 
 
-@pytest.mark.parametrize("bits", [1, 2, 4, 8, 16])
-@pytest.mark.parametrize("out", ["f32", "bf16"])
-def test_allgather_decode_many_rows_per_cta(bits, out):
-    # More than eight rows per CTA (2,600 rows of 4096 over at most 456 CTAs),
-    # so that the bf16 decode's four-row register ring is refilled several
-    # times and wraps around a ragged last row.
-    torch, bc = need_gpu()
-    rng = np.random.default_rng(bits + (7 if out == "bf16" else 0))
-    n = 2600 * 4096 + 77
-    codes, scales = _random_codes(rng, n, bits, 128)
-    cg = Guarded(torch, codes.size, fill=codes)
+# Smallest code-pointer alignment the ABI accepts per width, and the one the
+# 16-element all-gather-side decode needs (twice that, 8 bytes for 12 bits);
+# 16-bit codes need 16 bytes on both paths.
+CODE_ALIGN = {1: 1, 2: 2, 4: 4, 8: 8, 12: 4, 16: 16}
+
+
+def _dequant_case(torch, bc, rng, n, bits, block, out, mul, code_off=0, out_off=0):
+    """Decode random codes through the ABI with the codes placed code_off bytes
+    and the output out_off bytes past an aligned address; compare every output
+    element with the oracle and check that nothing outside the output moved."""
+    codes, scales = _random_codes(rng, n, bits, block)
+    cg = Guarded(torch, code_off + codes.size, fill=np.concatenate([np.zeros(code_off, np.uint8), codes]))
     sg = Guarded(torch, 2 * scales.size, fill=scales)
-    og = Guarded(torch, (4 if out == "f32" else 2) * n)
-    dst = og.view(torch.float32 if out == "f32" else torch.bfloat16)
-    mul = float(np.float32(1 / 8))
-    bc.unpack_dequant(cg.view(torch.uint8), sg.view(torch.int16), n, bc.QParams(bits, 128), mul, out=dst)
+    esz = 4 if out == "f32" else 2
+    og = Guarded(torch, out_off + esz * n)
+    dst = og.view(torch.uint8)[out_off:].view(torch.float32 if out == "f32" else torch.bfloat16)
+    bc.unpack_dequant(cg.view(torch.uint8)[code_off:], sg.view(torch.int16), n, bc.QParams(bits, block), mul,
+                      out=dst)
     torch.cuda.synchronize()
     assert og.guards_intact()
-    ref = O.unpack_dequant(codes, scales, n, O.params(bits, 128), mul, O.F32 if out == "f32" else O.BF16)
-    assert np.array_equal(og.host(np.uint32 if out == "f32" else np.uint16),
-                          ref.view(np.uint32 if out == "f32" else np.uint16))
+    raw = og.host(np.uint8)
+    assert (raw[:out_off] == 0xA5).all(), "bytes before the output changed"
+    ref = O.unpack_dequant(codes, scales, n, O.params(bits, block), mul, O.F32 if out == "f32" else O.BF16)
+    got = raw[out_off:].view(np.uint32 if out == "f32" else np.uint16)
+    assert np.array_equal(got, ref.view(np.uint32 if out == "f32" else np.uint16)), \
+        f"n={n} bits={bits} block={block} code_off={code_off} out_off={out_off}"
+
+
+@pytest.mark.parametrize("bits", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("path", ["wide", "narrow"])
+def test_allgather_decode_many_rows_per_cta(bits, out, path):
+    # 2,600 rows of 4096 elements and a ragged last row.  "wide" takes the
+    # 16-element kernel (about three rows per CTA); "narrow" places the output
+    # (bf16) or the codes (fp32) off that kernel's alignment, so the persistent
+    # 8-element kernel decodes more than eight rows per CTA and the bf16
+    # decode's four-row register ring is refilled several times and wraps
+    # around the ragged row.
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(bits + (7 if out == "bf16" else 0) + (100 if path == "narrow" else 0))
+    code_off = out_off = 0
+    if path == "narrow":
+        if out == "bf16":
+            out_off = 16
+        elif bits != 16:
+            code_off = CODE_ALIGN[bits]
+        else:
+            pytest.skip("16-bit codes into fp32 always meet the 16-element kernel's alignment")
+    _dequant_case(torch, bc, rng, 2600 * 4096 + 77, bits, 128, out, float(np.float32(1 / 8)), code_off, out_off)
+
+
+@pytest.mark.parametrize("bits", BITS)
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_allgather_decode_ragged_and_alignment_paths(bits, out):
+    # Ragged sizes (inside the first piece, at a piece and a row boundary, one
+    # past them), blocks from the smallest the 16-element kernel takes (16) to
+    # 4096 and 8 (the 8-element kernel only); codes at the smallest accepted
+    # alignment and an output 16 bytes off a 32-byte boundary (bf16) send the
+    # call to the 8-element kernel.  Every path gives the oracle's bits.
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(1000 + bits * 2 + (out == "bf16"))
+    mul = float(np.float32(1 / 3))
+    layouts = [(0, 0)]
+    if bits != 16:
+        layouts.append((CODE_ALIGN[bits], 0))
+    if out == "bf16":
+        layouts.append((0, 16))
+    for block in (8, 16, 64, 4096):
+        for n in (1, 15, 16, 17, 4096, 4096 + 16 * 5 + 7, 3 * 4096 + 1):
+            for code_off, out_off in layouts:
+                _dequant_case(torch, bc, rng, n, bits, block, out, mul, code_off, out_off)
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
