@@ -301,7 +301,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "inputs larger than L2 (%.1f GB of gradients per step)" % (W * n * 2 / 1e9),
                    "input_gbs_bf16": round(W * n * 2 * world / (step_ms * 1e-3) / 1e9, 2),
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
-        "roofline": {"bound": "hbm", "kernel": "encode_kernel<bf16,4,ef,rtn>",
+        "roofline": {"bound": "hbm", "kernel": "encode16_kernel<bf16,4,ef,rtn>",
                      "achieved": round(enc_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(enc_gbs / peak, 4), "peak_kind": peak_kind,
                      "traffic": traffic, "bytes_per_launch": enc_bytes,
@@ -428,7 +428,8 @@ def run_sharded(args, rank, world, local_rank):
                    "buckets": len(ar.buckets), "bucket_bytes": args.bucket_mb << 20,
                    "l2": "inputs larger than L2 (%.1f GB of gradient per rank)" % (n * 2 / 1e9),
                    "parallelism": f"sharded low-bit all-reduce over NCCL, {world} ranks (all-to-all + all-gather)"},
-        "roofline": {"bound": "hbm", "kernel": "encode_kernel<bf16,4,ef,rtn> (all buckets of one step)",
+        "roofline": {"bound": "hbm", "kernel": ("encode16_kernel<bf16,4,ef,rtn>" if args.bucket_mb == 0 else
+                                "encode_kernel or encode16_kernel<bf16,4,ef,rtn> by bucket size (all buckets of one step)"),
                      "achieved": round(enc_gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(enc_gbs / peak, 4),
                      "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": n * ENC_BYTES_PER_ELEM,
                      "launch_ms": round(enc_ms, 4)},
@@ -798,7 +799,7 @@ def run_workload(args):
                "warmup": warm, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
                "config": {"workload": wl.name, "n": wl.n, "input_dtype": "f32",
                           "l2": "inputs larger than L2 (1.07 GB)", "value_is": "encoder, 4-bit, block 128, RTN"},
-               "roofline": {"bound": "hbm", "kernel": "encode_kernel<f32,4,noef,rtn>",
+               "roofline": {"bound": "hbm", "kernel": "encode16_kernel<f32,4,noef,rtn>",
                             "achieved": head["encode_gbs"], "peak": peak, "unit": "GB/s",
                             "frac": head["encode_frac"], "peak_kind": peak_kind},
                "best_encode_input_gbs": best["encode_input_gbs"], "sweep": lines}

@@ -14,6 +14,7 @@
 
 #include "codec.cuh"
 #include "launch.h"
+#include "wide16.cuh"
 
 namespace bitscom {
 
@@ -149,71 +150,15 @@ __global__ void __launch_bounds__(kThreads, 2) dequant_kernel(const DqArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// 16 elements per thread.  The decode writes 4-16x the bytes it reads, and a
-// persistent grid-stride loop measured well below what plain writes reach:
-// on 2^29 elements (L2 flushed), stores alone from one CTA per resident slot
-// moved 0.93 of the measured copy bandwidth and from a grid 4-8x larger
-// 1.04-1.08.  So each CTA of this kernel decodes about three rows (the next
-// row's codes loaded before the current row's store) and the grid holds
-// rows / 3 CTAs, never fewer than the GPU holds at once: every width into
-// bf16 or fp32, 2^29 and 1.3e9 elements, 0.98-1.04 of measured HBM (the
-// persistent 8-element kernel 0.60-0.98; one or two rows per CTA 0.77-0.94 for
-// 1-bit codes, 8 rows 0.96-1.03; a ring of rows in registers and 512-thread
-// CTAs made no difference).
-constexpr int kDq16Threads = 256;
-constexpr int kDq16Row = kDq16Threads * 16;
+// 16 elements per thread (wide16.cuh).  The decode writes 4-16x the bytes it
+// reads; each CTA decodes about three rows (the next row's codes loaded before
+// the current row's store) and the grid holds rows / 3 CTAs, never fewer than
+// the GPU holds at once: every width into bf16 or fp32, 2^29 and 1.3e9
+// elements, 0.98-1.04 of measured HBM (the persistent 8-element kernel
+// 0.60-0.98; one or two rows per CTA 0.77-0.94 for 1-bit codes, 8 rows
+// 0.96-1.03; a ring of rows in registers and 512-thread CTAs made no
+// difference).
 constexpr int kDq16RowsPerCta = 3;
-
-// Codes of 16 consecutive elements (two 8-element pieces), one load of 2b
-// bytes (two for 12 and 16 bits).  e0 is a multiple of 16 below n: with
-// blocks of >= 16 the packed codes cover whole blocks, so all 16 elements'
-// codes are inside the buffer even when n ends inside them.
-template <int BITS>
-struct Codes16 { Packed<BITS> c[2]; };
-
-// one 32-byte store of eight words (p 32-byte aligned)
-__device__ __forceinline__ void st8_b32(void* p, const uint32_t (&w)[8])
-{
-    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                 :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]),
-                    "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-}
-
-template <int BITS>
-__device__ __forceinline__ Codes16<BITS> load_codes16(const uint8_t* codes, int64_t e0)
-{
-    Codes16<BITS> t;
-    const uint8_t* p = codes + (e0 >> 3) * BITS;
-    if constexpr (BITS == 1) {
-        const uint32_t w = __ldg(reinterpret_cast<const unsigned short*>(p));
-        t.c[0].w[0] = w & 0xFFu;
-        t.c[1].w[0] = w >> 8;
-    } else if constexpr (BITS == 2) {
-        const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(p));
-        t.c[0].w[0] = w & 0xFFFFu;
-        t.c[1].w[0] = w >> 16;
-    } else if constexpr (BITS == 4) {
-        const uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
-        t.c[0].w[0] = w.x;
-        t.c[1].w[0] = w.y;
-    } else if constexpr (BITS == 8) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
-        t.c[0].w[0] = w.x; t.c[0].w[1] = w.y;
-        t.c[1].w[0] = w.z; t.c[1].w[1] = w.w;
-    } else if constexpr (BITS == 12) {
-        const uint2* q = reinterpret_cast<const uint2*>(p);
-        const uint2 w0 = __ldg(q), w1 = __ldg(q + 1), w2 = __ldg(q + 2);
-        t.c[0].w[0] = w0.x; t.c[0].w[1] = w0.y; t.c[0].w[2] = w1.x;
-        t.c[1].w[0] = w1.y; t.c[1].w[1] = w2.x; t.c[1].w[2] = w2.y;
-    } else {
-        const uint4* q = reinterpret_cast<const uint4*>(p);
-        const uint4 w0 = __ldg(q), w1 = __ldg(q + 1);
-        t.c[0].w[0] = w0.x; t.c[0].w[1] = w0.y; t.c[0].w[2] = w0.z; t.c[0].w[3] = w0.w;
-        t.c[1].w[0] = w1.x; t.c[1].w[1] = w1.y; t.c[1].w[2] = w1.z; t.c[1].w[3] = w1.w;
-    }
-    return t;
-}
 
 // y = fl(fl(s*q) * mul) for one piece.  s*q is exact in fp32 for every width
 // (an fp16 scale times a level of at most 16 bits), so the packed-fp16 levels
@@ -247,30 +192,24 @@ __device__ __forceinline__ void piece_values(const Packed<BITS>& c, unsigned sho
     }
 }
 
-__device__ __forceinline__ uint32_t bf16_pair(float lo, float hi)
-{
-    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&b);
-}
-
 // Thread t of a CTA decodes elements [16t, 16t + 16) of rows blockIdx.x + k G.
 template <int BITS, int OUT>
-__global__ void __launch_bounds__(kDq16Threads) dequant16_kernel(const DqArgs a)
+__global__ void __launch_bounds__(kWideThreads) dequant16_kernel(const DqArgs a)
 {
     const int64_t n = a.n;
-    const int64_t rows = (n + kDq16Row - 1) / kDq16Row;
+    const int64_t rows = (n + kWideRow - 1) / kWideRow;
     const int64_t G = gridDim.x;
     Codes16<BITS> c{};
     unsigned short s = 0;
     auto load = [&](int64_t row) {
-        const int64_t e0 = row * kDq16Row + (int64_t)threadIdx.x * 16;
+        const int64_t e0 = row * kWideRow + (int64_t)threadIdx.x * 16;
         if (row >= rows || e0 >= n) return;
         c = load_codes16<BITS>(a.codes, e0);
         s = __ldg(a.scales + (e0 >> a.log2B));
     };
     load(blockIdx.x);
     for (int64_t row = blockIdx.x; row < rows; row += G) {
-        const int64_t e0 = row * kDq16Row + (int64_t)threadIdx.x * 16;
+        const int64_t e0 = row * kWideRow + (int64_t)threadIdx.x * 16;
         float y0[8], y1[8];
         piece_values<BITS>(c.c[0], s, a.mul, y0);
         piece_values<BITS>(c.c[1], s, a.mul, y1);
@@ -305,19 +244,11 @@ __global__ void __launch_bounds__(kDq16Threads) dequant16_kernel(const DqArgs a)
     }
 }
 
-// Code alignment the 16-element loads need: twice the 8-element piece's
-// load width (two 8-byte loads for 12 bits).
-template <int BITS>
-__host__ __device__ constexpr uintptr_t dq16_code_align()
-{
-    return BITS == 1 ? 2 : (BITS == 2 ? 4 : (BITS == 4 ? 8 : (BITS == 12 ? 8 : 16)));
-}
-
 template <int BITS>
 static bool dq16_fits(const DqArgs& a)
 {
     return a.hadamard == 0 && a.log2B >= 4 &&
-           (reinterpret_cast<uintptr_t>(a.codes) & (dq16_code_align<BITS>() - 1)) == 0 &&
+           (reinterpret_cast<uintptr_t>(a.codes) & (code16_align<BITS>() - 1)) == 0 &&
            (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;
 }
 
@@ -325,22 +256,9 @@ template <int BITS, int OUT>
 static cudaError_t run_dequant16(const DqArgs& a, cudaStream_t st)
 {
     static std::atomic<int> resident{0};
-    int c = resident.load(std::memory_order_relaxed);
-    if (c == 0) {
-        int dev = 0, occ = 0, sms = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dequant16_kernel<BITS, OUT>, kDq16Threads, 0);
-        c = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
-        resident.store(c, std::memory_order_relaxed);
-    }
-    const int64_t rows = (a.n + kDq16Row - 1) / kDq16Row;
-    const int64_t spread = (rows + kDq16RowsPerCta - 1) / kDq16RowsPerCta;
-    const int64_t full = rows < c ? rows : c;
-    int64_t g = spread > full ? spread : full;
-    if (g > 0x7FFFFFFF) g = 0x7FFFFFFF;          // the grid-stride loop covers the rest
-    const int grid = (int)g;
-    dequant16_kernel<BITS, OUT><<<grid, kDq16Threads, 0, st>>>(a);
+    const int64_t rows = (a.n + kWideRow - 1) / kWideRow;
+    const int grid = spread_grid(dequant16_kernel<BITS, OUT>, kWideThreads, resident, rows, kDq16RowsPerCta, 1);
+    dequant16_kernel<BITS, OUT><<<grid, kWideThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 

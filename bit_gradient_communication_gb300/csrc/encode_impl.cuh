@@ -372,27 +372,60 @@ __global__ void __launch_bounds__(kThreads16, 3) encode16_kernel(const EncArgs a
     }
 }
 
+// Grids of the encoders (spread_grid): about this many rows per CTA when the
+// launch spans at least kEncSpreadWaves waves of resident CTAs, else the
+// persistent grid.  Measured on 1.3e9 bf16 and 2^28 fp32 elements (L2
+// flushed, fractions of measured HBM), against the persistent grid:
+//   16-element kernel, error feedback, round to nearest: 2 rows per CTA,
+//     every width and block 1.05 (0.97-0.99 persistent with the 8-element
+//     kernel, 0.90-0.95 persistent with this one); 3 rows 1.04, 8 rows 1.03;
+//   16-element kernel without error feedback: 8 rows per CTA, fp32 4-bit
+//     0.95 (0.88), 16-bit 1.01 (1.00), bf16 4-bit 0.89 (0.82);
+//   8-element kernel with error feedback (stochastic rounding, the rotated
+//     encoders, 12-bit codes): 8 rows per CTA, fp32 2- and 4-bit stochastic
+//     rounding 1.03 (0.93), bf16 2-bit 0.997 (0.96), 8-bit with Hadamard
+//     H = 128 0.992 (0.972); 3-4 rows per CTA measured up to 1.04 on the fp32
+//     cases but 0.96-0.97 on the bf16 and rotated ones.  Without error
+//     feedback (its two-buffer loop, read-heavy: fp32 12-bit codes) it stays
+//     persistent: 8 rows per CTA measured 0.91-1.00 against 0.93-1.02.
+// On 5e7 elements the 16-element error-feedback kernel at 2 rows per CTA
+// (13 waves) still won (0.960 against 0.937); 8 rows per CTA of the 8-element
+// kernel (5 waves) lost (0.893).
+constexpr int kEncSpreadWaves = 12;
+constexpr int kEnc16EfRowsPerCta = 2;
+constexpr int kEnc16RowsPerCta = 8;
+constexpr int kEnc8RowsPerCta = 8;
+
+// The memory-bound round-to-nearest encoders of 4- to 16-bit codes without
+// error feedback measured faster on a persistent grid with three CTAs per SM
+// than with the four their registers allow (fp32, 2^28 elements: 16-bit 1.01
+// against 0.86-0.91 of measured HBM, 4- and 8-bit 0.97-0.98 against
+// 0.95-0.96); 1- and 2-bit codes run as many as fit.
+template <bool SR, bool DEQ, int BITS>
+constexpr int enc16_occ_cap() { return (!SR && !DEQ && BITS >= 4) ? 3 : 0; }
+
+// The 16-element kernel takes round to nearest with error feedback only over
+// a spread grid: on a persistent grid it measured below the 8-element kernel
+// (5e7 elements 0.872 against 0.937; fp32 25 MiB buckets 0.59-0.64 against
+// 0.65-0.70).
+template <int IN, int BITS>
+static bool encode16_ef_spreads(const EncArgs& a)
+{
+    static std::atomic<int> res{0};
+    const int c = resident_ctas(encode16_kernel<IN, BITS, true, false, false>, kThreads16, res,
+                                enc16_occ_cap<false, false, BITS>());
+    const int64_t rows = (a.n + kRow - 1) / kRow;
+    return (rows + kEnc16EfRowsPerCta - 1) / kEnc16EfRowsPerCta >= (int64_t)kEncSpreadWaves * c;
+}
+
 template <int IN, int BITS, bool EF, bool SR, bool DEQ = false>
 static cudaError_t run_encode16(const EncArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};
     const int64_t rows = (a.n + kRow - 1) / kRow;
-    int c = cap.load(std::memory_order_relaxed);
-    if (c == 0) {
-        int dev = 0, occ = 0, sms = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, encode16_kernel<IN, BITS, EF, SR, DEQ>, kThreads16, 0);
-        // The memory-bound round-to-nearest encoders of 4- to 16-bit codes
-        // measured faster with three CTAs per SM than with the four their
-        // registers allow (fp32, 2^28 elements: 16-bit 1.01 against 0.86-0.91
-        // of measured HBM, 4- and 8-bit 0.97-0.98 against 0.95-0.96); 1- and
-        // 2-bit codes run as many as fit.
-        if constexpr (!SR && !DEQ && BITS >= 4) occ = occ < 3 ? occ : 3;
-        c = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
-        cap.store(c, std::memory_order_relaxed);
-    }
-    const int grid = (int)(rows < c ? rows : c);
+    const int grid = spread_grid(encode16_kernel<IN, BITS, EF, SR, DEQ>, kThreads16, cap, rows,
+                                 EF ? kEnc16EfRowsPerCta : kEnc16RowsPerCta, kEncSpreadWaves,
+                                 enc16_occ_cap<SR, DEQ, BITS>());
     EncArgs b = a;
     b.pack_mul = BITS <= 8 ? (1u << BITS) : 0u;
     encode16_kernel<IN, BITS, EF, SR, DEQ><<<grid, kThreads16, 0, st>>>(b);
@@ -410,7 +443,9 @@ static cudaError_t run_encode_h(const EncArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};   // SMs x resident CTAs of this instantiation
     const int64_t rows = (a.n + kRow - 1) / kRow;
-    const int grid = grid_size(encode_kernel<IN, BITS, EF, SR, HAD>, cap, rows);
+    const int grid = EF ? spread_grid(encode_kernel<IN, BITS, EF, SR, HAD>, kThreads, cap, rows, kEnc8RowsPerCta,
+                                      kEncSpreadWaves)
+                        : grid_size(encode_kernel<IN, BITS, EF, SR, HAD>, cap, rows);
     encode_kernel<IN, BITS, EF, SR, HAD><<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
@@ -427,10 +462,15 @@ static cudaError_t run_encode(const EncArgs& a, cudaStream_t st)
                 return IN == 0 ? launch_encode32_sr_f32(a, BITS, st) : launch_encode32_sr_bf16(a, BITS, st);
         }
     }
-    // without error feedback only: with it, the 16-element layout spills and
-    // measured slower on the 25 MiB fp32 buckets (0.59-0.64 vs 0.65-0.70)
     if constexpr (!EF && BITS != 12) {
         if (encode16_fits(a, BITS)) return run_encode16<IN, BITS, EF, SR>(a, st);
+    }
+    // error feedback with round to nearest: the 16-element kernel when the
+    // launch is large enough for a spread grid (with stochastic rounding it
+    // spills: 1.01 against 1.04 for the 8-element kernel on 2^28 fp32)
+    if constexpr (EF && !SR && BITS != 12) {
+        if (encode16_fits(a, BITS) && encode16_ef_spreads<IN, BITS>(a))
+            return run_encode16<IN, BITS, true, false>(a, st);
     }
     if (a.hadamard == 0) return run_encode_h<IN, BITS, EF, SR, false>(a, st);
     if constexpr (BITS == 2 || BITS == 4 || BITS == 8) {

@@ -8,11 +8,14 @@
 //            the same way (optionally writing the weights as fp32 or bf16), so
 //            all copies stay bit-identical and the residual w - ref carries
 //            over to the next step.
-// Both kernels use the row / piece / team decomposition of codec.cuh and are
-// software-pipelined like the encoder.
+// The encoder and the 8-element apply use the row / piece / team
+// decomposition of codec.cuh and are software-pipelined like the encoder; the
+// 16-element apply (blocks of >= 16, codes and weights aligned for its wider
+// accesses) runs over a grid of short-lived CTAs (wide16.cuh).
 #include <cuda_bf16.h>
 
 #include "encode_impl.cuh"
+#include "wide16.cuh"
 
 namespace bitscom {
 
@@ -126,13 +129,14 @@ __global__ void __launch_bounds__(kThreads, 2) qwd_apply_kernel(const QwdApplyAr
         for (int j = 0; j < 8; ++j) r[j] = nref[j];
         uint32_t h[4];
         level_pairs<BITS>(cur, h);
+        const unsigned short s = cur_s;          // this row's scale: load() below replaces cur_s
         __syncthreads();   // the CTA's next-row loads reach DRAM together (0.925 -> 0.960)
         if (row + gridDim.x < rows) load(row + gridDim.x);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int jl = pair_lo<BITS>(i), jh = pair_hi<BITS>(i);
-            r[jl] = fma_f16(cur_s, (unsigned short)(h[i] & 0xFFFFu), r[jl]);   // fl(ref + s*q)
-            r[jh] = fma_f16(cur_s, (unsigned short)(h[i] >> 16), r[jh]);
+            r[jl] = fma_f16(s, (unsigned short)(h[i] & 0xFFFFu), r[jl]);   // fl(ref + s*q)
+            r[jh] = fma_f16(s, (unsigned short)(h[i] >> 16), r[jh]);
         }
         if (valid == 8) {
             st8_f32(a.ref + e0, r);
@@ -167,12 +171,87 @@ __global__ void __launch_bounds__(kThreads, 2) qwd_apply_kernel(const QwdApplyAr
     }
 }
 
+// 16 elements per thread, about two rows per CTA.  The apply reads 4.5 and
+// writes 4-8 bytes per element; on 1.3e9 4-bit elements in groups of 2048
+// (L2 flushed) it measured 1.04-1.05 of measured HBM with bf16 weights out or
+// none (the persistent 8-element kernel 0.96 / 0.92; that kernel with a grid of
+// rows / 3 CTAs 0.98 / 0.94; three to eight rows per CTA 1.03-1.04; loading the
+// next row one iteration ahead made no difference).
+constexpr int kApply16RowsPerCta = 2;
+
+template <int BITS, int WOUT>
+__global__ void __launch_bounds__(kWideThreads) qwd_apply16_kernel(const QwdApplyArgs a)
+{
+    const int64_t n = a.n;
+    const int64_t rows = (n + kWideRow - 1) / kWideRow;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t e0 = row * kWideRow + (int64_t)threadIdx.x * 16;
+        if (e0 >= n) continue;
+        const int64_t rem = n - e0;
+        const Codes16<BITS> c = load_codes16<BITS>(a.codes, e0);
+        const unsigned short s = __ldg(a.scales + (e0 >> a.log2B));
+        float r0[8], r1[8];
+        if (rem >= 16) {
+            ld8_f32(a.ref + e0, r0);
+            ld8_f32(a.ref + e0 + 8, r1);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                r0[j] = j < rem ? a.ref[e0 + j] : 0.0f;
+                r1[j] = j + 8 < rem ? a.ref[e0 + 8 + j] : 0.0f;
+            }
+        }
+        uint32_t h0[4], h1[4];
+        level_pairs<BITS>(c.c[0], h0);
+        level_pairs<BITS>(c.c[1], h1);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int jl = pair_lo<BITS>(i), jh = pair_hi<BITS>(i);
+            r0[jl] = fma_f16(s, (unsigned short)(h0[i] & 0xFFFFu), r0[jl]);     // fl(ref + s*q)
+            r0[jh] = fma_f16(s, (unsigned short)(h0[i] >> 16), r0[jh]);
+            r1[jl] = fma_f16(s, (unsigned short)(h1[i] & 0xFFFFu), r1[jl]);
+            r1[jh] = fma_f16(s, (unsigned short)(h1[i] >> 16), r1[jh]);
+        }
+        if (rem >= 16) {
+            st8_f32(a.ref + e0, r0);
+            st8_f32(a.ref + e0 + 8, r1);
+            if constexpr (WOUT == 1) {
+                float* w = static_cast<float*>(a.w_out) + e0;
+                st8_f32(w, r0);
+                st8_f32(w + 8, r1);
+            } else if constexpr (WOUT == 2) {
+                uint32_t wv[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    wv[i] = bf16_pair(r0[2 * i], r0[2 * i + 1]);
+                    wv[4 + i] = bf16_pair(r1[2 * i], r1[2 * i + 1]);
+                }
+                st8_b32(static_cast<uint16_t*>(a.w_out) + e0, wv);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (j < rem) {
+                    const float v = j < 8 ? r0[j] : r1[j - 8];
+                    a.ref[e0 + j] = v;
+                    if constexpr (WOUT == 1) static_cast<float*>(a.w_out)[e0 + j] = v;
+                    if constexpr (WOUT == 2)
+                        static_cast<uint16_t*>(a.w_out)[e0 + j] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+                }
+            }
+        }
+    }
+}
+
 template <int IN, int BITS, bool SR>
 static cudaError_t run_qwd_encode(const EncArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};
     const int64_t rows = (a.n + kRow - 1) / kRow;
-    const int grid = grid_size(qwd_encode_kernel<IN, BITS, SR>, cap, rows);
+    // the sender moves the bytes of an error-feedback encoder; it takes that
+    // encoder's spread grid (encode_impl.cuh)
+    const int grid = spread_grid(qwd_encode_kernel<IN, BITS, SR>, kThreads, cap, rows, kEnc8RowsPerCta,
+                                 kEncSpreadWaves);
     qwd_encode_kernel<IN, BITS, SR><<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
@@ -196,6 +275,15 @@ cudaError_t launch_qwd_encode(const EncArgs& a, int dtype, int bits, bool sr, cu
 template <int BITS, int WOUT>
 static cudaError_t run_qwd_apply(const QwdApplyArgs& a, cudaStream_t st)
 {
+    if (a.log2B >= 4 && (reinterpret_cast<uintptr_t>(a.codes) & (code16_align<BITS>() - 1)) == 0 &&
+        (reinterpret_cast<uintptr_t>(a.w_out) & 31u) == 0) {        // ref: 32-byte aligned by contract
+        static std::atomic<int> resident{0};
+        const int64_t rows = (a.n + kWideRow - 1) / kWideRow;
+        const int grid =
+            spread_grid(qwd_apply16_kernel<BITS, WOUT>, kWideThreads, resident, rows, kApply16RowsPerCta, 1);
+        qwd_apply16_kernel<BITS, WOUT><<<grid, kWideThreads, 0, st>>>(a);
+        return cudaGetLastError();
+    }
     static std::atomic<int> cap{0};
     const int64_t rows = (a.n + kRow - 1) / kRow;
     const int grid = grid_size(qwd_apply_kernel<BITS, WOUT>, cap, rows);

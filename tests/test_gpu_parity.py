@@ -787,6 +787,49 @@ def test_qwd_matches_oracle_over_steps(dt, bits, block, rounding):
         assert np.array_equal(wout.view(torch.int16).cpu().numpy().view(np.uint16), w_ref), f"step {t}"
 
 
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("wout", ["none", "f32", "bf16"])
+def test_qwd_apply_ragged_and_alignment_paths(bits, wout):
+    # The receiver's apply on random codes: ragged sizes, blocks 8 (the
+    # 8-element kernel only), 16 and 2048, codes at the smallest accepted
+    # alignment and bf16 weights 16 bytes off a 32-byte boundary (both send
+    # the call to the 8-element kernel), and 2,600 rows (several rows per CTA
+    # on either kernel).  The reference and the weights match the oracle bit
+    # for bit and nothing outside them is written.
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(500 + bits * 3 + len(wout))
+    layouts = [(0, 0), (CODE_ALIGN[bits], 0)] + ([(0, 16)] if wout == "bf16" else [])
+    cases = [(b, n) for b in (8, 16, 2048) for n in (1, 15, 17, 4096 + 16 * 3 + 5)] + [(2048, 2600 * 4096 + 77)]
+    for block, n in cases:
+        for code_off, out_off in layouts:
+            codes, scales = _random_codes(rng, n, bits, block)
+            ref0 = rng.standard_normal(n).astype(np.float32)
+            cg = Guarded(torch, code_off + codes.size, fill=np.concatenate([np.zeros(code_off, np.uint8), codes]))
+            sg = Guarded(torch, 2 * scales.size, fill=scales)
+            rg = Guarded(torch, 4 * n, fill=ref0)
+            og = None
+            dst = None
+            if wout != "none":
+                esz = 4 if wout == "f32" else 2
+                og = Guarded(torch, out_off + esz * n)
+                dst = og.view(torch.uint8)[out_off:].view(torch.float32 if wout == "f32" else torch.bfloat16)
+            bc.qwd_apply(cg.view(torch.uint8)[code_off:], sg.view(torch.int16), n, bc.QParams(bits, block),
+                         rg.view(torch.float32), dst)
+            torch.cuda.synchronize()
+            h_ref = ref0.copy()
+            w_ref = O.qwd_apply(codes, scales, n, O.params(bits, block), h_ref,
+                                O.BF16 if wout == "bf16" else O.F32)
+            tag = f"n={n} block={block} code_off={code_off} out_off={out_off}"
+            assert rg.guards_intact(), tag
+            assert np.array_equal(rg.host(np.uint32), h_ref.view(np.uint32)), tag
+            if og is not None:
+                assert og.guards_intact(), tag
+                raw = og.host(np.uint8)
+                assert (raw[:out_off] == 0xA5).all(), tag
+                got = raw[out_off:].view(np.uint32 if wout == "f32" else np.uint16)
+                assert np.array_equal(got, w_ref.view(np.uint32 if wout == "f32" else np.uint16)), tag
+
+
 @pytest.mark.parametrize("wout", ["none", "f32"])
 def test_qwd_apply_weight_outputs(wout):
     # The receiver's apply without a weight copy and with an fp32 one (the
