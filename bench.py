@@ -54,15 +54,16 @@ DEC_BYTES_PER_ELEM = W_RANKS * (BITS / 8 + 2 / BLOCK) + 4 + 4 + BITS / 8 + 2 / B
 # device; each encoder launch moves 0.63 GB, five times the L2), caches left
 # alone between launches (ncu --cache-control none), averaged over the step's
 # 8 encoder and 8 decoder launches; the step's total equals its algorithmic
-# bytes to 0.07 % (the last encoder's dirty lines are written back, and
+# bytes to 0.1 % (the last encoder's dirty lines are written back, and
 # counted, during the first decoder), and the bytes per element do not depend
 # on the size once it is well above the L2 (2e8 per rank gave 10.5057 and
-# 12.6902 on earlier sources).
+# 12.6902 on earlier sources).  At 6e7 per rank the encoder launch already
+# takes the same spread grid as at full size (sixteen waves of two-row CTAs).
 TRAFFIC_SOURCES = ("launch.h", "codec.cuh", "encode_impl.cuh", "encode_bf16.cu", "decode_impl.cuh",
                    "decode_w8.cu")
 NCU_TRAFFIC = {
-    "encode": {"src": "fa211e8b87f23073", "bytes_per_elem": 10.4920},
-    "decode": {"src": "fa211e8b87f23073", "bytes_per_elem": 12.7664},
+    "encode": {"src": "4af21214b9d43990", "bytes_per_elem": 10.4931},
+    "decode": {"src": "4af21214b9d43990", "bytes_per_elem": 12.7272},
 }
 
 
