@@ -7,12 +7,16 @@
 // ranks in order, so every implementation gets the same bits (a collective's
 // own reduction order is unspecified).
 //
-// HBM-bound streaming kernel: a persistent grid walks 8-element pieces (a
-// warp's loads of one rank are 512 or 1024 contiguous bytes); a thread loads
-// its piece of every rank (256-bit loads for fp32, 128-bit for bf16) and writes
-// one 256-bit store.  For W = 2, 4 or 8 (sum_fixed_kernel) every rank's load is
-// in flight before the first add; other W (sum_ranks_kernel) load four ranks
-// at a time.  (Pieces of 16 bf16 elements, two 128-bit loads per rank 32 bytes
+// HBM-bound streaming kernel: a grid of 256-thread CTAs walks 8-element
+// pieces (a warp's loads of one rank are 512 or 1024 contiguous bytes); a
+// thread loads its piece of every rank (256-bit loads for fp32, 128-bit for
+// bf16) and writes one 256-bit store.  For W = 2, 4 or 8 (sum_fixed_kernel)
+// every rank's load is in flight before the first add, over a spread grid of
+// one 2048-element stretch per CTA for large launches (spread_grid in
+// codec.cuh: W = 8 bf16, 1.3e9 elements, 1.06 of the measured copy bandwidth
+// against 0.986 on a persistent grid; two to sixteen stretches per CTA
+// 1.04-1.05); other W (sum_ranks_kernel) load four ranks at a time on a
+// persistent grid.  (Pieces of 16 bf16 elements, two 128-bit loads per rank 32 bytes
 // apart, measured 0.58 of the copy bandwidth on the W = 8 node-local reduce of
 // a 1.3e9-element gradient, against 0.835 for four ranks in flight.)
 #include "codec.cuh"
@@ -124,22 +128,19 @@ __global__ void __launch_bounds__(kSumThreads) sum_fixed_kernel(const SumArgs a)
     }
 }
 
+// one grid-stride stretch (kSumThreads pieces) per CTA once the launch spans
+// twelve waves of resident CTAs, as the encoders' spread grids
+constexpr int kSumStretchesPerCta = 1;
+constexpr int kSumSpreadWaves = 12;
+
 template <int IN, int W>
 static cudaError_t run_sum_fixed(const SumArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};
-    int c = cap.load(std::memory_order_relaxed);
-    if (c == 0) {
-        int dev = 0, occ = 0, sms = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sum_fixed_kernel<IN, W>, kSumThreads, 0);
-        c = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
-        cap.store(c, std::memory_order_relaxed);
-    }
     const int64_t pieces = (a.n + 7) >> 3;
     const int64_t blocks = (pieces + kSumThreads - 1) / kSumThreads;
-    const int grid = (int)(blocks < c ? blocks : c);
+    const int grid = spread_grid(sum_fixed_kernel<IN, W>, kSumThreads, cap, blocks, kSumStretchesPerCta,
+                                 kSumSpreadWaves);
     sum_fixed_kernel<IN, W><<<grid, kSumThreads, 0, st>>>(a);
     return cudaGetLastError();
 }

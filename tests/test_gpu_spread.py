@@ -4,7 +4,8 @@ CTAs): the 16-element encoder with error feedback and round to nearest
 (every bf16 width, fp32), a launch just below its threshold (the 8-element
 kernel's persistent grid), the 8-element kernel with stochastic rounding and
 with the Walsh-Hadamard rotation, the 16-element encoder without error
-feedback, the one-pass roundtrip and the weight-difference sender.  The sizes
+feedback, the one-pass roundtrip, the weight-difference sender and the
+rank-ordered sum of the full-precision local reduce.  The sizes
 leave a margin of 1.4x or more on either side of the thresholds for a
 152-SM GB300; every code, scale, error and output element is compared with
 the CPU oracle, and guard bands around every output must survive."""
@@ -126,3 +127,27 @@ def test_qwd_sender_spread():
     assert codes.cpu().numpy().tobytes() == c_ref.tobytes()
     assert np.array_equal(scales.cpu().numpy().view(np.uint16), s_ref)
     assert np.array_equal(rg.host(np.uint32), h_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("dt,W", [("bf16", 4), ("f32", 2)])
+def test_sum_ranks_spread(dt, W):
+    # 4.2e7 elements: 20,508 stretches of 2,048 (one per CTA; twelve waves of
+    # at most eight 256-thread CTAs on each of 152 SMs are 14,592), a ragged
+    # last piece
+    torch, bc = need_gpu()
+    n = 42_000_003
+    rng = np.random.default_rng(40 + W)
+    xs = []
+    for w in range(W):
+        x = rng.standard_normal(n, dtype=np.float32) * np.float32(10.0 ** (w - 2))
+        x[rng.integers(0, n, 64)] = -0.0
+        xs.append(x if dt == "f32" else bf16_bits_of(torch, x))
+    ref = O.sum_ranks(xs)
+    dev = [torch.from_numpy(x if dt == "f32" else x.view(np.int16)).cuda() for x in xs]
+    if dt == "bf16":
+        dev = [d.view(torch.bfloat16) for d in dev]
+    out = Guarded(torch, 4 * n)
+    bc.sum_ranks(dev, out=out.view(torch.float32))
+    torch.cuda.synchronize()
+    assert out.guards_intact()
+    assert np.array_equal(out.host(np.uint32), ref.view(np.uint32))
