@@ -438,21 +438,26 @@ __global__ void __launch_bounds__(kThreads16, 3) decode16_w8_kernel(const DecArg
     }
 }
 
+// Grids of the decoders (spread_grid in codec.cuh).  Each CTA loads its next
+// row while it finishes the current one, so a CTA needs several rows for that
+// to pay: on 1.3e9 outputs (sum only) and 1.625e8 (8 -> 4 bits, 8 ranks),
+// fractions of measured HBM, one row per CTA measured 0.89-0.90, eight 0.998
+// and 1.021-1.026, sixteen 1.005 and 1.002, thirty-two 0.99 and 0.96, against
+// 0.983 and 0.994 on a persistent grid.  The requantising 4 -> 4-bit
+// 16-element decoder measured the same at eight rows per CTA (0.969) and
+// slower at sixteen or more (0.944-0.950), and keeps its persistent grid.
+constexpr int kDecSpreadWaves = 12;
+constexpr int kDec16SumRowsPerCta = 16;
+constexpr int kDec8RowsPerCta = 8;
+
 template <bool SR, bool REQ = true, int TW = 0>
 static cudaError_t run_decode16_w8(const DecArgs& a, cudaStream_t st)
 {
     static std::atomic<int> cap{0};
     const int64_t rows = (a.n + kRow - 1) / kRow;
-    int c = cap.load(std::memory_order_relaxed);
-    if (c == 0) {
-        int dev = 0, occ = 0, sms = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode16_w8_kernel<SR, REQ, TW>, kThreads16, 0);
-        c = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
-        cap.store(c, std::memory_order_relaxed);
-    }
-    const int grid = (int)(rows < c ? rows : c);
+    const int grid = REQ ? grid_size_threads(decode16_w8_kernel<SR, REQ, TW>, kThreads16, cap, rows)
+                         : spread_grid(decode16_w8_kernel<SR, REQ, TW>, kThreads16, cap, rows, kDec16SumRowsPerCta,
+                                       kDecSpreadWaves);
     decode16_w8_kernel<SR, REQ, TW><<<grid, kThreads16, 0, st>>>(a);
     return cudaGetLastError();
 }
@@ -499,7 +504,8 @@ static cudaError_t run_decode_kw(const DecArgs& a, cudaStream_t st)
     }
     static std::atomic<int> cap{0};
     const int64_t rows = (a.n + kRow - 1) / kRow;
-    const int grid = grid_size(decode_kernel<BIN, BOUT, SR, MANY, KW>, cap, rows);
+    const int grid = spread_grid(decode_kernel<BIN, BOUT, SR, MANY, KW>, kThreads, cap, rows, kDec8RowsPerCta,
+                                 kDecSpreadWaves);
     decode_kernel<BIN, BOUT, SR, MANY, KW><<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }

@@ -4,11 +4,16 @@ CTAs): the 16-element encoder with error feedback and round to nearest
 (every bf16 width, fp32), a launch just below its threshold (the 8-element
 kernel's persistent grid), the 8-element kernel with stochastic rounding and
 with the Walsh-Hadamard rotation, the 16-element encoder without error
-feedback, the one-pass roundtrip, the weight-difference sender and the
-rank-ordered sum of the full-precision local reduce.  The sizes
+feedback, the one-pass roundtrip, the weight-difference sender, the
+rank-ordered sum of the full-precision local reduce, and the decoders whose
+grids spread (eight ranks 8 -> 4 bits, and the eight-rank sum alone).  The
+sizes
 leave a margin of 1.4x or more on either side of the thresholds for a
 152-SM GB300; every code, scale, error and output element is compared with
-the CPU oracle, and guard bands around every output must survive."""
+the CPU oracle (the decoders on block-aligned windows: every output block
+depends only on the same block of every rank and on its own stage-2 error,
+so a window is a complete oracle problem), and guard bands around every
+output must survive."""
 import numpy as np
 import pytest
 
@@ -151,3 +156,82 @@ def test_sum_ranks_spread(dt, W):
     torch.cuda.synchronize()
     assert out.guards_intact()
     assert np.array_equal(out.host(np.uint32), ref.view(np.uint32))
+
+
+def _random_ranks(torch, n, bits, block, seed, W=8):
+    """W ranks of random codes and fp16 scales (with some zero scales) on the
+    device, from a seeded device generator."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    nbytes = (n + block - 1) // block * block * bits // 8
+    nb = (n + block - 1) // block
+    codes, scales = [], []
+    for _ in range(W):
+        codes.append(torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device="cuda", generator=g))
+        s = (torch.randn(nb, device="cuda", generator=g).abs() * 1e-3).half()
+        s[torch.randint(0, nb, (max(1, nb // 50),), device="cuda", generator=g)] = 0.0
+        scales.append(s.view(torch.int16))
+    return codes, scales
+
+
+def _windows(n, unit, count, seed):
+    """Block-aligned windows [lo, hi) of 16 units: the first, the last (ragged
+    when n is) and `count` others."""
+    nu = (n + unit - 1) // unit
+    rng = np.random.default_rng(seed)
+    starts = {0, max(0, nu - 16)} | set(int(v) for v in rng.integers(0, max(1, nu - 16), count))
+    return [(b * unit, min((b + 16) * unit, n)) for b in sorted(starts)]
+
+
+def _host(t, lo, hi):
+    return t[lo:hi].cpu().numpy()
+
+
+def test_decoder_8_to_4_spread():
+    # 1.6e8 + 1,613 outputs of eight ranks' 8-bit codes in blocks of 512,
+    # requantised to 4 bits in blocks of 128 with stage-2 error: 40,961 rows,
+    # 5,121 CTAs of eight rows (twelve waves of 304 resident are 3,648)
+    torch, bc = need_gpu()
+    n = 160 * 2 ** 20 + 1613
+    p_in, p_out = bc.QParams(8, 512), bc.QParams(4, 128)
+    codes, scales = _random_ranks(torch, n, 8, 512, 7)
+    e2_0 = torch.randn(n, device="cuda") * 1e-6
+    e2 = Guarded(torch, 4 * n)
+    e2.view(torch.float32).copy_(e2_0)
+    co = Guarded(torch, bc.packed_bytes(n, 4, 128))
+    so = Guarded(torch, 2 * bc.num_blocks(n, 128))
+    bc.unpack_dequant_reduce_requant(codes, scales, n, p_in, err2=e2.view(torch.float32), p_out=p_out,
+                                     codes_out=co.view(torch.uint8), scales_out=so.view(torch.int16))
+    torch.cuda.synchronize()
+    assert e2.guards_intact() and co.guards_intact() and so.guards_intact()
+    e2_out, co_out, so_out = e2.view(torch.float32), co.view(torch.uint8), so.view(torch.int16)
+    for lo, hi in _windows(n, 512, 12, 3):
+        m = hi - lo
+        cw = [_host(c, lo, lo + (m + 511) // 512 * 512) for c in codes]
+        sw = [_host(sc, lo // 512, lo // 512 + (m + 511) // 512).view(np.uint16) for sc in scales]
+        ew = _host(e2_0, lo, hi).copy()
+        _, c_ref, s_ref = O.unpack_dequant_reduce_requant(cw, sw, m, O.params(8, 512), False, ew, O.params(4, 128))
+        assert _host(co_out, lo // 2, lo // 2 + c_ref.size).tobytes() == c_ref.tobytes(), f"codes at {lo}"
+        assert np.array_equal(_host(so_out, lo // 128, lo // 128 + s_ref.size).view(np.uint16), s_ref), f"scales at {lo}"
+        assert np.array_equal(_host(e2_out, lo, hi).view(np.uint32), ew.view(np.uint32)), f"e2 at {lo}"
+
+
+def test_sum_only_decoder_spread():
+    # 5.2e8 + 77 outputs, the sum of eight ranks' 4-bit codes in blocks of
+    # 128 (the 16-element kernel without requantisation): 126,954 rows, 7,935
+    # CTAs of sixteen rows (twelve waves of 456 resident are 5,472)
+    torch, bc = need_gpu()
+    n = 520_000_077
+    p = bc.QParams(4, 128)
+    codes, scales = _random_ranks(torch, n, 4, 128, 8)
+    out = Guarded(torch, 4 * n)
+    bc.unpack_dequant_reduce_requant(codes, scales, n, p, sum_out=out.view(torch.float32))
+    torch.cuda.synchronize()
+    assert out.guards_intact()
+    sums = out.view(torch.float32)
+    for lo, hi in _windows(n, 128, 16, 4):
+        m = hi - lo
+        cw = [_host(c, lo // 2, (lo + (m + 127) // 128 * 128) // 2) for c in codes]
+        sw = [_host(sc, lo // 128, lo // 128 + (m + 127) // 128).view(np.uint16) for sc in scales]
+        ref, _, _ = O.unpack_dequant_reduce_requant(cw, sw, m, O.params(4, 128), True)
+        assert np.array_equal(_host(sums, lo, hi).view(np.uint32), ref.view(np.uint32)), f"sum at {lo}"
