@@ -845,10 +845,11 @@ def run_workload(args):
         algo = wl.n * (12 + 0.5 + 2 / wl.block)
         extra = {"l2": "flushed between timed iterations (256 MB write, then 256 MB read); warm_l2_* without it",
                  "per_bits": per_bits, "value_is": "4-bit, L2 flushed"}
-    elif args.workload == "allgather_decode_gpt1p3b":
-        # every rank's decode of the all-gathered 4-bit codes into its bf16 mean gradient
+    elif args.workload in ("allgather_decode_gpt1p3b", "allgather_decode_hs_gpt1p3b"):
+        # every rank's decode of the all-gathered 4-bit codes into its bf16 mean
+        # gradient (with the inverse rotation for the Hadamard-smoothed codes)
         x = synth.gradients(wl.kind, wl.n, wl.seed, dtype=dt, **wl.params)
-        p = bc.QParams(wl.bits, wl.block)
+        p = bc.QParams(wl.bits, wl.block, hadamard=wl.hadamard)
         codes, scales = bc.quantize_pack(x, p)
         out = torch.empty(wl.n, dtype=torch.bfloat16, device="cuda")
         step = lambda: bc.unpack_dequant(codes, scales, wl.n, p, 1.0 / wl.ranks, out)
@@ -856,7 +857,8 @@ def run_workload(args):
             step()
         t = _timed(torch, step, K)
         algo = wl.n * (wl.bits / 8 + 2 / wl.block + 2)
-        extra = {"l2": "inputs larger than L2 (3.3 GB per step)", "output": "bf16", "mul": "1/8"}
+        extra = {"l2": "inputs larger than L2 (3.3 GB per step)", "output": "bf16", "mul": "1/8",
+                 "hadamard": wl.hadamard}
     elif args.workload == "tlq_hs_w8_gpt1p3b":
         # two-level quantisation with Hadamard smoothing: stage 1 8-bit groups of
         # 512, stage 2 4-bit groups of 128, both rotated by H = 128

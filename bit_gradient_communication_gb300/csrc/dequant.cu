@@ -5,11 +5,13 @@
 // fp32 or bf16 (round to nearest even).  One read of the codes and scales,
 // one write of the output.
 //
-// Two kernels.  dequant16_kernel (blocks of >= 16, no rotation, codes and
+// Three kernels.  dequant16_kernel (blocks of >= 16, no rotation, codes and
 // output aligned for its wider accesses) decodes 16 elements per thread with
-// 32-byte stores over a grid of many short-lived CTAs; dequant_kernel takes
-// every other case, 8 elements per thread over a persistent grid with the
-// row loop software-pipelined like the encoder's.
+// 32-byte stores over a grid of many short-lived CTAs; dequant32h_kernel
+// takes the rotated decode when the blocks hold >= 32 elements (32 elements
+// per thread, so up to five of the transform's stages stay in registers);
+// dequant_kernel takes every other case, 8 elements per thread over a
+// persistent grid with the row loop software-pipelined like the encoder's.
 #include <cuda_bf16.h>
 
 #include "codec.cuh"
@@ -262,6 +264,218 @@ static cudaError_t run_dequant16(const DqArgs& a, cudaStream_t st)
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// The rotated decode with 32 elements per thread (blocks of >= 32).  The inverse
+// transform is the forward one (stages h = 1, 2, ..., H/2, pair (i, i + h)
+// -> (x_i + x_{i+h}, x_i - x_{i+h})) followed by the exact factor 1/H, as in
+// fwht8.  With 8 elements per thread every stage from h = 8 on is a round of
+// xor shuffles, one per element, and each round measured ~62 us per 2^29
+// elements: H = 128 into bf16 took 478 us, 0.42 of measured HBM.  Here the
+// stages h = 1..16 (up to H/2 for H = 8 and 16) run in registers on packed
+// pairs and only log2(H/32) rounds cross threads, each a shuffle per element and one packed fma per
+// pair (k x + o with k = +1 on the lower lane and -1 on the upper: the same
+// single rounding as x + o and o - x).  bf16 output is stored directly, one
+// 32-byte store per 16 elements; fp32 output goes through shared memory so
+// that every store instruction of a warp writes 1 KB contiguous (the direct
+// 128 bytes per thread measured 0.72-0.84 of measured HBM, the staged stores
+// 0.97-0.99).  2^29 elements, bf16 / fp32 out: H = 32 0.97 / 0.98, 64 0.87 /
+// 0.98, 128 0.75-0.88 / 0.98-0.99, 256 0.56 / 0.82 (the 8-element kernel
+// 0.57 / 0.88, 0.48 / 0.77, 0.42-0.51 / 0.69-0.78, 0.32 / 0.61).  Staging the
+// bf16 stores measured slower (0.67-0.95): there the shuffles and the
+// arithmetic, not the stores, set the pace.
+constexpr int kH32Threads = 256;
+constexpr int kH32Row = kH32Threads * 32;
+constexpr int kH32RowsPerCta = 4;
+constexpr int kH32StageWords = 36;                  // padded row of the fp32 staging buffer
+
+template <int BITS>
+struct Codes32h { Packed<BITS> c[4]; };
+
+// codes of 32 consecutive elements (e0 a multiple of 32): 8, 16 or 32 bytes
+template <int BITS>
+__device__ __forceinline__ Codes32h<BITS> load_codes32(const uint8_t* codes, int64_t e0)
+{
+    Codes32h<BITS> t;
+    const uint8_t* p = codes + (e0 >> 3) * BITS;
+    if constexpr (BITS == 2) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
+        t.c[0].w[0] = w.x & 0xFFFFu; t.c[1].w[0] = w.x >> 16;
+        t.c[2].w[0] = w.y & 0xFFFFu; t.c[3].w[0] = w.y >> 16;
+    } else if constexpr (BITS == 4) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
+        t.c[0].w[0] = w.x; t.c[1].w[0] = w.y; t.c[2].w[0] = w.z; t.c[3].w[0] = w.w;
+    } else {
+        const uint4* q = reinterpret_cast<const uint4*>(p);
+        const uint4 w0 = __ldg(q), w1 = __ldg(q + 1);
+        t.c[0].w[0] = w0.x; t.c[0].w[1] = w0.y; t.c[1].w[0] = w0.z; t.c[1].w[1] = w0.w;
+        t.c[2].w[0] = w1.x; t.c[2].w[1] = w1.y; t.c[3].w[0] = w1.z; t.c[3].w[1] = w1.w;
+    }
+    return t;
+}
+
+// one in-register stage of span HS over 32 values, two butterflies per pair
+// of packed instructions (a + b, and a - b as the fma -b + a)
+template <int HS>
+__device__ __forceinline__ void wht_stage32(float (&x)[32])
+{
+    const float2 m1 = make_float2(-1.0f, -1.0f);
+    if constexpr (HS == 1) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            const float2 a = make_float2(x[j], x[j + 2]), b = make_float2(x[j + 1], x[j + 3]);
+            const float2 s = __fadd2_rn(a, b), d = __ffma2_rn(b, m1, a);
+            x[j] = s.x; x[j + 2] = s.y; x[j + 1] = d.x; x[j + 3] = d.y;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            if (j & HS) continue;
+            const float2 a = make_float2(x[j], x[j + 1]), b = make_float2(x[j + HS], x[j + HS + 1]);
+            const float2 s = __fadd2_rn(a, b), d = __ffma2_rn(b, m1, a);
+            x[j] = s.x; x[j + 1] = s.y; x[j + HS] = d.x; x[j + HS + 1] = d.y;
+        }
+    }
+}
+
+// Thread t decodes elements [32t, 32t + 32) of rows blockIdx.x + k G.  n is a
+// multiple of H.  SMALL = false (H >= 32): the H/32 threads of a transform
+// block are all in or all out of range, and out-of-range threads still take
+// part in the shuffles.  SMALL = true (H = 8 or 16): no stage crosses threads,
+// and the last thread may hold whole transform blocks beyond n, which it
+// computes from the padding of its codes block and does not store.  (One
+// kernel for both, with the stages and the ragged stores chosen at run time,
+// took 68-74 registers and measured 0.61 instead of 0.75 for H = 128.)
+template <int BITS, int OUT, bool SMALL>
+__global__ void __launch_bounds__(kH32Threads) dequant32h_kernel(const DqArgs a)
+{
+    __shared__ __align__(16) float stage[OUT == 0 ? kH32Threads * kH32StageWords : 4];
+    const int64_t n = a.n;
+    const int64_t rows = (n + kH32Row - 1) / kH32Row;
+    const int lane = threadIdx.x & 31;
+    const int H = a.hadamard;
+    const float inv = 1.0f / (float)H;                         // a power of two: exact
+    const float2 inv2 = make_float2(inv, inv), mul2 = make_float2(a.mul, a.mul);
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t e0 = row * kH32Row + (int64_t)threadIdx.x * 32;
+        const bool active = e0 < n;
+        float v[32];
+        if (active) {
+            const Codes32h<BITS> c = load_codes32<BITS>(a.codes, e0);
+            const unsigned short s = __ldg(a.scales + (e0 >> a.log2B));     // blocks of >= H >= 32
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                uint32_t h[4];
+                level_pairs<BITS>(c.c[p], h);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[8 * p + pair_lo<BITS>(i)] = fma_f16(s, (unsigned short)(h[i] & 0xFFFFu), -0.0f);
+                    v[8 * p + pair_hi<BITS>(i)] = fma_f16(s, (unsigned short)(h[i] >> 16), -0.0f);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+        }
+        wht_stage32<1>(v);
+        wht_stage32<2>(v);
+        wht_stage32<4>(v);
+        if constexpr (SMALL) {
+            if (H == 16) wht_stage32<8>(v);
+        } else {
+            wht_stage32<8>(v);
+            wht_stage32<16>(v);
+        }
+        for (int m = 1; m < (SMALL ? 1 : (H >> 5)); m <<= 1) {
+            const float k = (lane & m) ? -1.0f : 1.0f;
+            const float2 k2 = make_float2(k, k);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const float o0 = __shfl_xor_sync(0xFFFFFFFFu, v[j], m);
+                const float o1 = __shfl_xor_sync(0xFFFFFFFFu, v[j + 1], m);
+                const float2 r = __ffma2_rn(make_float2(v[j], v[j + 1]), k2, make_float2(o0, o1));
+                v[j] = r.x;
+                v[j + 1] = r.y;
+            }
+        }
+        // out = fl(fl(d / H) * mul), each rounded as the scalar multiply
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            const float2 t = __fmul2_rn(__fmul2_rn(make_float2(v[j], v[j + 1]), inv2), mul2);
+            v[j] = t.x;
+            v[j + 1] = t.y;
+        }
+        if constexpr (OUT == 0) {
+            // lane l's 32 values into row l of its warp's buffer, then store
+            // instruction q takes elements [256 q, 256 q + 256) of the warp's
+            // 1024 (row 8q + l/4, words 8 (l % 4) .. + 8); the padded rows keep
+            // both the writes and the reads free of bank conflicts
+            float* buf = stage + (threadIdx.x >> 5) * (32 * kH32StageWords);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<float4*>(buf + lane * kH32StageWords + 4 * i) =
+                    make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            __syncwarp();
+            const int64_t wbase = row * kH32Row + (int64_t)(threadIdx.x & ~31) * 32;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float* src = buf + (8 * q + (lane >> 2)) * kH32StageWords + 8 * (lane & 3);
+                const float4 t0 = *reinterpret_cast<const float4*>(src);
+                const float4 t1 = *reinterpret_cast<const float4*>(src + 4);
+                const float w[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+                const int64_t o = wbase + 256 * q + 8 * lane;
+                if (!SMALL || o + 8 <= n) {
+                    if (o < n) st8_f32(static_cast<float*>(a.out) + o, w);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) if (o + j < n) static_cast<float*>(a.out)[o + j] = w[j];
+                }
+            }
+            __syncwarp();
+        } else {
+            if (!active) continue;
+            uint16_t* out = static_cast<uint16_t*>(a.out) + e0;
+            if (!SMALL || e0 + 32 <= n) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) w[i] = bf16_pair(v[16 * q + 2 * i], v[16 * q + 2 * i + 1]);
+                    st8_b32(out + 16 * q, w);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (e0 + j < n) out[j] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+            }
+        }
+    }
+}
+
+template <int BITS>
+static bool dq32h_fits(const DqArgs& a)
+{
+    constexpr uintptr_t ca = BITS == 2 ? 8 : 16;
+    return a.hadamard >= 8 && a.log2B >= 5 && (reinterpret_cast<uintptr_t>(a.codes) & (ca - 1)) == 0 &&
+           (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;
+}
+
+template <int BITS, int OUT, bool SMALL>
+static cudaError_t run_dequant32h_s(const DqArgs& a, cudaStream_t st)
+{
+    static std::atomic<int> resident{0};
+    const int64_t rows = (a.n + kH32Row - 1) / kH32Row;
+    const int grid =
+        spread_grid(dequant32h_kernel<BITS, OUT, SMALL>, kH32Threads, resident, rows, kH32RowsPerCta, 1);
+    dequant32h_kernel<BITS, OUT, SMALL><<<grid, kH32Threads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int BITS, int OUT>
+static cudaError_t run_dequant32h(const DqArgs& a, cudaStream_t st)
+{
+    return a.hadamard >= 32 ? run_dequant32h_s<BITS, OUT, false>(a, st) : run_dequant32h_s<BITS, OUT, true>(a, st);
+}
+
 template <int BITS, int OUT, bool HAD>
 static cudaError_t run_dequant_h(const DqArgs& a, cudaStream_t st)
 {
@@ -278,6 +492,7 @@ static cudaError_t run_dequant(const DqArgs& a, cudaStream_t st)
     if (dq16_fits<BITS>(a)) return run_dequant16<BITS, OUT>(a, st);
     if (a.hadamard == 0) return run_dequant_h<BITS, OUT, false>(a, st);
     if constexpr (BITS == 2 || BITS == 4 || BITS == 8) {
+        if (dq32h_fits<BITS>(a)) return run_dequant32h<BITS, OUT>(a, st);
         return run_dequant_h<BITS, OUT, true>(a, st);
     } else {
         return cudaErrorNotSupported;

@@ -89,6 +89,7 @@ class Workload:
     bucket_bytes: int = 0
     seed: int = 0
     sr_seed: int = 0
+    hadamard: int = 0           # Walsh-Hadamard transform block H, 0 = none
 
 
 MiB = 1024 * 1024
@@ -114,6 +115,12 @@ WORKLOADS = {
                                bits=4, block=2048, ranks=8, seed=7),
     "allgather_decode_gpt1p3b": Workload("allgather_decode_gpt1p3b", 1_300_000_000, "bf16", "normal",
                                          {"sigma": 1e-3}, bits=4, block=128, ranks=8, seed=1000),
+    # the same decode of the two-level Hadamard-smoothed all-reduce's stage-2
+    # codes (4-bit blocks of 128, rotated by H = 128): the inverse rotation runs
+    # in the decode
+    "allgather_decode_hs_gpt1p3b": Workload("allgather_decode_hs_gpt1p3b", 1_300_000_000, "bf16", "normal",
+                                            {"sigma": 1e-3}, bits=4, block=128, ranks=8, seed=1000,
+                                            hadamard=128),
     "sweep_laplace_256m": Workload("sweep_laplace_256m", 268_435_456, "f32", "laplace", {"b": 1e-3},
                                    bits=4, block=128, seed=5, sr_seed=55),
     # pipeline-A without local quantisation: the node leader's rank-ordered fp32

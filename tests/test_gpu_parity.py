@@ -642,7 +642,7 @@ def test_allgather_decode_matches_oracle(bits, block, out):
 CODE_ALIGN = {1: 1, 2: 2, 4: 4, 8: 8, 12: 4, 16: 16}
 
 
-def _dequant_case(torch, bc, rng, n, bits, block, out, mul, code_off=0, out_off=0):
+def _dequant_case(torch, bc, rng, n, bits, block, out, mul, code_off=0, out_off=0, hadamard=0):
     """Decode random codes through the ABI with the codes placed code_off bytes
     and the output out_off bytes past an aligned address; compare every output
     element with the oracle and check that nothing outside the output moved."""
@@ -652,13 +652,14 @@ def _dequant_case(torch, bc, rng, n, bits, block, out, mul, code_off=0, out_off=
     esz = 4 if out == "f32" else 2
     og = Guarded(torch, out_off + esz * n)
     dst = og.view(torch.uint8)[out_off:].view(torch.float32 if out == "f32" else torch.bfloat16)
-    bc.unpack_dequant(cg.view(torch.uint8)[code_off:], sg.view(torch.int16), n, bc.QParams(bits, block), mul,
-                      out=dst)
+    bc.unpack_dequant(cg.view(torch.uint8)[code_off:], sg.view(torch.int16), n,
+                      bc.QParams(bits, block, hadamard=hadamard), mul, out=dst)
     torch.cuda.synchronize()
     assert og.guards_intact()
     raw = og.host(np.uint8)
     assert (raw[:out_off] == 0xA5).all(), "bytes before the output changed"
-    ref = O.unpack_dequant(codes, scales, n, O.params(bits, block), mul, O.F32 if out == "f32" else O.BF16)
+    ref = O.unpack_dequant(codes, scales, n, O.params(bits, block, hadamard=hadamard), mul,
+                           O.F32 if out == "f32" else O.BF16)
     got = raw[out_off:].view(np.uint32 if out == "f32" else np.uint16)
     assert np.array_equal(got, ref.view(np.uint32 if out == "f32" else np.uint16)), \
         f"n={n} bits={bits} block={block} code_off={code_off} out_off={out_off}"
@@ -707,6 +708,26 @@ def test_allgather_decode_ragged_and_alignment_paths(bits, out):
         for n in (1, 15, 16, 17, 4096, 4096 + 16 * 5 + 7, 3 * 4096 + 1):
             for code_off, out_off in layouts:
                 _dequant_case(torch, bc, rng, n, bits, block, out, mul, code_off, out_off)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("H", [8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_rotated_decode_paths(bits, H, out):
+    # The rotated all-gather-side decode with blocks of >= 32 elements (32
+    # elements per thread, the fp32 output staged through shared memory): 41
+    # rows of 8192 and a ragged last row (for H = 8 and 16 ending inside a
+    # thread's 32 elements), a single transform block, and codes at the
+    # smallest accepted alignment or a bf16 output 16 bytes off a 32-byte
+    # boundary, which take the 8-element kernel instead.
+    torch, bc = need_gpu()
+    rng = np.random.default_rng(3000 + bits * 10 + H + (out == "bf16"))
+    block = max(H, 128)
+    mul = float(np.float32(1 / 3))
+    layouts = [(0, 0), (CODE_ALIGN[bits], 0)] + ([(0, 16)] if out == "bf16" else [])
+    for n in (41 * 8192 + 3 * H, H):
+        for code_off, out_off in layouts:
+            _dequant_case(torch, bc, rng, n, bits, block, out, mul, code_off, out_off, hadamard=H)
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])

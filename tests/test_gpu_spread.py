@@ -235,3 +235,31 @@ def test_sum_only_decoder_spread():
         sw = [_host(sc, lo // 128, lo // 128 + (m + 127) // 128).view(np.uint16) for sc in scales]
         ref, _, _ = O.unpack_dequant_reduce_requant(cw, sw, m, O.params(4, 128), True)
         assert np.array_equal(_host(sums, lo, hi).view(np.uint32), ref.view(np.uint32)), f"sum at {lo}"
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_rotated_decode_spread(out):
+    # The all-gather-side decode with the inverse Walsh-Hadamard rotation
+    # (H = 128, 4-bit blocks of 128) over 4e7 elements: 4,883 rows of 8192,
+    # four rows per CTA, the fp32 output staged through shared memory; every
+    # transform block depends only on its own codes and scale, so block-aligned
+    # windows are complete oracle problems
+    torch, bc = need_gpu()
+    n = 40_000_000
+    p = bc.QParams(4, 128, hadamard=128)
+    po = O.params(4, 128, hadamard=128)
+    codes, scales = _random_ranks(torch, n, 4, 128, 21, W=1)
+    esz = 4 if out == "f32" else 2
+    g = Guarded(torch, esz * n)
+    mul = float(np.float32(1 / 8))
+    bc.unpack_dequant(codes[0], scales[0], n, p, mul, out=g.view(torch.float32 if out == "f32" else torch.bfloat16))
+    torch.cuda.synchronize()
+    assert g.guards_intact()
+    res = g.view(torch.int32 if out == "f32" else torch.int16)
+    for lo, hi in _windows(n, 128, 16, 5):
+        m = hi - lo
+        cw = _host(codes[0], lo // 2, hi // 2)
+        sw = _host(scales[0], lo // 128, hi // 128).view(np.uint16)
+        ref = O.unpack_dequant(cw, sw, m, po, mul, O.F32 if out == "f32" else O.BF16)
+        got = _host(res, lo, hi).view(np.uint32 if out == "f32" else np.uint16)
+        assert np.array_equal(got, ref.view(np.uint32 if out == "f32" else np.uint16)), f"window at {lo}"
