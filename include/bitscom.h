@@ -171,6 +171,13 @@ bitscom_status bitscom_unpack_dequant_reduce_requant(
  * is a SUM; mul = 1/W turns it into the mean.
  *   codes, scales   one stream of packed codes / fp16 scales of n elements for
  *                   p (alignment as the encoder's outputs).
+ * Performance note: with blocks of >= 16, no rotation, codes aligned to twice
+ * the encoder's store width and out 32-byte aligned, the decode handles 16
+ * elements per thread; with a rotation (p->hadamard != 0), blocks of >= 32,
+ * codes 8-byte (b = 2) or 16-byte (b = 4, 8) aligned and out 32-byte aligned,
+ * it handles 32 and keeps up to five stages of the transform in registers
+ * (H = 128 into bf16: 1.8x the 8-element kernel).  The results are the same
+ * bits on every path.
  */
 bitscom_status bitscom_unpack_dequant(const void* codes, const uint16_t* scales, int64_t n,
                                       const bitscom_qparams* p, float mul, bitscom_dtype out_dt,
@@ -209,7 +216,10 @@ bitscom_status bitscom_qwd_encode(const void* w, bitscom_dtype dt, int64_t n, fl
                                   const bitscom_qparams* p, void* codes_out, uint16_t* scales_out,
                                   void* cuda_stream);
 /* Receiver side: ref = fl(ref + fl(s*q)) for n elements of gathered codes;
- * w_out (NULL = none) receives the new weights as fp32 or bf16 (w_dt). */
+ * w_out (NULL = none) receives the new weights as fp32 or bf16 (w_dt).
+ * Performance note: with blocks of >= 16, codes aligned to twice the encoder's
+ * store width and w_out 32-byte aligned (or NULL), the apply handles 16
+ * elements per thread; the results are the same bits on every path. */
 bitscom_status bitscom_qwd_apply(const void* codes, const uint16_t* scales, int64_t n,
                                  const bitscom_qparams* p, float* ref, void* w_out,
                                  bitscom_dtype w_dt, void* cuda_stream);
