@@ -168,6 +168,7 @@ class AllReduceW8:
         self.codes, self.scales = zip(*[bc.alloc_codes(n, self.p1[0], device) for _ in range(W)])
         self.err2 = torch.zeros(n, dtype=torch.float32, device=device)
         self.codes_out, self.scales_out = bc.alloc_codes(n, self.p2, device)
+        self.side = torch.cuda.Stream(device=device)   # the second stream of decode()
         B1, B2 = self.p1[0].block, self.p2.block
         U = max(B1, B2)                          # chunks are whole blocks of both stages
         units = (n + U - 1) // U
@@ -188,8 +189,21 @@ class AllReduceW8:
                               stream=stream)
 
     def decode(self, stream=None):
+        """The W chunk decoders, alternately on the caller's stream and a second
+        one (joined back before return).  They read the encoders' outputs and
+        write disjoint chunks, so their order does not matter; on two streams one
+        decoder's last wave overlaps the next one's first (8 x 1.625e8 outputs:
+        2.55 -> 2.46 ms for the eight, the same bits)."""
+        torch = self.torch
+        main = stream or torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(main)
+        self.side.wait_event(fork)
         for c in range(len(self.chunks)):
-            self.decode_chunk(c, stream)
+            self.decode_chunk(c, main if c % 2 == 0 else self.side)
+        join = torch.cuda.Event()
+        join.record(self.side)
+        main.wait_event(join)
 
     def decode_chunk(self, c, stream=None):
         """Chunk c's decoder: the W ranks' codes of chunk c (what the all-to-all
